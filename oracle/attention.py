@@ -223,7 +223,9 @@ def combine_splits(o_parts, lse_parts):
     total = w.sum(axis=0)
     lse = np.where(finite, m_safe + np.log(np.where(finite, total, 1.0)), -np.inf)
     coef = np.where(finite, w / np.where(finite, total, 1.0), 0.0)
-    out = (coef[..., None] * o_parts).sum(axis=0)
+    # an empty split's partial output is undefined and is never read
+    live = np.isfinite(lse_parts)[..., None]
+    out = np.where(live, coef[..., None] * np.where(live, o_parts, 0.0), 0.0).sum(axis=0)
     return out, lse
 
 

@@ -270,6 +270,11 @@ def test_combine_with_empty_splits():
     np.testing.assert_allclose(out[0], (w0 * o[0, 0] + w2 * o[2, 0]) / (w0 + w2), atol=1e-12)
     assert abs(l[0] - math.log(w0 + w2)) < 1e-12
     assert np.all(out[1] == 0) and np.isneginf(l[1])
+    # the partial output of an empty split is never read (it may hold anything)
+    o_nan = o.copy()
+    o_nan[1, 0] = np.nan
+    out2, _ = oracle.combine_splits(o_nan, lse)
+    assert np.array_equal(out2, out)
 
 
 def test_causal_prefix_equals_stepwise_decode():
