@@ -1,0 +1,404 @@
+"""Benchmark: paged KV-cache decode on one GB300 (plus replicas for N > 1).
+
+One step = one serving decode step of the paged path: append the new token's
+k/v into its page and attend over the paged cache (page resolution, fused
+append, device split plan, split-KV decode and, when splits are used, the
+combine) for a batch of 256 sequences at context 4096 with 32 query / 32 kv
+heads, head_dim 128, fp16, 16-token pages and a block table that is a random
+permutation of the pool.  The cache (17.2 GB) is far larger than L2 (129 MB),
+so no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is the whole-job algorithmic HBM
+throughput in GB/s; `roofline` compares the decode kernel's achieved GB/s with
+the measured HBM copy bandwidth; `cpu_baseline` is the CPU oracle timed on a
+bounded sample of the same workload.  `--impl reference` times the CPU oracle
+itself as the reference arm.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(workload="paged decode step with fused 1-token append", batch=256, ctx=4096,
+                num_q_heads=32, num_kv_heads=32, head_dim=128, page_size=16, dtype="f16",
+                lnew=1, block_table="random permutation of the pool", values="N(0,1)",
+                l2="inputs (17.2 GB of K/V) larger than L2; no flush")
+METRIC = "paged decode HBM GB/s (% of peak) and prefill TFLOPS (% tensor peak) vs µs/call"
+
+
+def algorithmic_bytes(B, lk, lnew, lq, hq, hkv, d, elt=2):
+    """Bytes the step must move at minimum: every key/value of the context once
+    (cached ones from HBM, new ones from k_new/v_new), the appended k/v write,
+    q, out, lse and the block-table entries."""
+    kv_read = B * lk * hkv * d * elt * 2
+    append_write = B * lnew * hkv * d * elt * 2
+    q_out = B * lq * hq * d * elt * 2
+    lse = B * lq * hq * 4
+    table = B * math.ceil(lk / 16) * 4
+    return kv_read + append_write + q_out + lse + table
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "pa_common.cuh", "pa_internal.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_page_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, or None if
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "decode_paged_b256_ctx4096.txt")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256_16") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_oracle_rate(w_cpu, seqs, lnew):
+    """Time the CPU oracle on sequences `seqs` of the workload; returns
+    (GB/s-equivalent, seconds, sample description)."""
+    import numpy as np
+
+    import oracle
+
+    q = w_cpu["q"]
+    t0 = time.perf_counter()
+    nbytes = 0
+    for b in seqs:
+        old = int(w_cpu["cache_seqlens"][b])
+        oracle.fwd_kvcache(q[b:b + 1], w_cpu["k_pages"][b], w_cpu["v_pages"][b], [old],
+                           np.arange(w_cpu["k_pages"][b].shape[0])[None],
+                           k_new=w_cpu["k_new"][b:b + 1], v_new=w_cpu["v_new"][b:b + 1],
+                           scale=w_cpu["scale"], causal=False)
+        nbytes += algorithmic_bytes(1, old + lnew, lnew, q.shape[1], q.shape[2],
+                                    w_cpu["k_new"].shape[2], q.shape[3])
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt
+
+
+def host_sample(w, seqs):
+    """Copy the pages of `seqs` to the host as float64 arrays for the oracle."""
+    table = w["block_table"]
+    out = {"q": w["q"].double().cpu().numpy(), "k_new": w["k_new"].double().cpu().numpy(),
+           "v_new": w["v_new"].double().cpu().numpy(), "cache_seqlens": w["cache_seqlens"].cpu(),
+           "scale": w["scale"], "k_pages": {}, "v_pages": {}}
+    for b in seqs:
+        npg = -(-int(w["cache_seqlens"][b]) // 16)
+        pages = table[b, :npg].long()
+        out["k_pages"][b] = w["k_cache"][pages].double().cpu().numpy()
+        out["v_pages"][b] = w["v_cache"][pages].double().cpu().numpy()
+    return out
+
+
+def cpu_baseline(w, budget_s=10.0):
+    import torch
+
+    lnew = WORKLOAD["lnew"]
+    probe = [0]
+    hs = host_sample(w, probe)
+    rate, dt = cpu_oracle_rate(hs, probe, lnew)
+    n = max(1, min(64, int(budget_s / max(dt, 1e-3))))
+    seqs = list(range(n))
+    hs = host_sample(w, seqs)
+    rate, dt = cpu_oracle_rate(hs, seqs, lnew)
+    del torch
+    return {"value": round(rate, 3), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {WORKLOAD['batch']} sequences (ctx {WORKLOAD['ctx']}, 32x128 "
+                      f"heads) through the float64 numpy oracle, {dt:.1f} s; cores = host "
+                      f"threads available to its BLAS"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle as it stands, on rank 0 only."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle  # noqa: F401
+    from paged_kv_cache_page_gb300 import workloads as wl
+
+    B = WORKLOAD["batch"]
+    # Draw the workload on the GPU when there is one (drawing 17 GB on the host
+    # takes minutes), else a smaller host draw of the same shape per sequence.
+    import torch
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    if dev == "cpu":
+        w = wl.paged_decode(8, WORKLOAD["ctx"], lnew=WORKLOAD["lnew"], seed=1002, device="cpu")
+    else:
+        w = wl.paged_decode(B, WORKLOAD["ctx"], lnew=WORKLOAD["lnew"], seed=1002, device=dev)
+    seqs_per_step = 2
+    total = args.warmup + args.steps
+    seqs = [i % w["q"].shape[0] for i in range(total * seqs_per_step)]
+    hs = host_sample(w, sorted(set(seqs)))
+    lnew = WORKLOAD["lnew"]
+    for i in range(args.warmup):
+        cpu_oracle_rate(hs, seqs[i * seqs_per_step:(i + 1) * seqs_per_step], lnew)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.warmup, total):
+        s = seqs[i * seqs_per_step:(i + 1) * seqs_per_step]
+        cpu_oracle_rate(hs, s, lnew)
+        nbytes += algorithmic_bytes(len(s), WORKLOAD["ctx"], lnew, lnew, 32, 32, 128)
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    line = {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": dict(WORKLOAD, sample=f"{seqs_per_step} sequences per step"),
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{seqs_per_step} of {B} sequences per step"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    del np
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, local = dist_env()
+
+    import torch
+    import torch.distributed as dist
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    import paged_kv_cache_page_gb300 as pa
+    from paged_kv_cache_page_gb300 import workloads as wl
+
+    pa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, ctx, lnew = WORKLOAD["batch"], WORKLOAD["ctx"], WORKLOAD["lnew"]
+    hq, hkv, d = WORKLOAD["num_q_heads"], WORKLOAD["num_kv_heads"], WORKLOAD["head_dim"]
+    # each rank is an independent replica with its own sequences (weak scaling)
+    w = wl.paged_decode(B, ctx, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, lnew=lnew,
+                        seed=1002 + rank, device=dev)
+    out = torch.empty((B, lnew, hq, d), dtype=torch.float16, device=dev)
+    lse = torch.empty((B, hq, lnew), dtype=torch.float32, device=dev)
+    ws_bytes = pa.fwd_kvcache_workspace_size(B, lnew, hq, hkv, d, ctx, 0)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    launches_per_step = 1 + (1 if ws_bytes > 0 else 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],
+                          w["block_table"], k=w["k_new"], v=w["v_new"], scale=w["scale"],
+                          out=out, lse=lse, workspace=ws, max_seqlen_k=ctx)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_all1.record(stream)
+        barrier()
+    elapsed_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    step_bytes = algorithmic_bytes(B, ctx, lnew, lnew, hq, hkv, d)
+    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+
+    # end-to-end through the public API with host buffers: inputs of the step
+    # (q, new k/v, lengths, block table) copied from pinned host memory, output
+    # and lse read back, every step.
+    h_q = w["q"].cpu().pin_memory()
+    h_k = w["k_new"].cpu().pin_memory()
+    h_v = w["v_new"].cpu().pin_memory()
+    h_sl = w["cache_seqlens"].cpu().pin_memory()
+    h_bt = w["block_table"].cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(w["q"]), torch.empty_like(w["k_new"]), torch.empty_like(w["v_new"])
+    d_sl, d_bt = torch.empty_like(w["cache_seqlens"]), torch.empty_like(w["block_table"])
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_sl, h_bt))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        pa.pa_fwd_kvcache(d_q, w["k_cache"], w["v_cache"], d_sl, d_bt, k=d_k, v=d_v,
+                          scale=w["scale"], out=out, lse=lse, workspace=ws, max_seqlen_k=ctx)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9
+
+    if rank == 0:
+        peak, peak_src = read_peaks()
+        achieved = step_bytes / (per_launch_ms * 1e-3) / 1e9
+        traffic = profiled_traffic()
+        cpu = None
+        if not args.no_cpu_baseline and world >= 1:
+            cpu = cpu_baseline(w)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": dict(WORKLOAD, parallelism=f"replicas x{world}",
+                           us_per_call=round(elapsed_ms / args.steps * 1e3, 2),
+                           algorithmic_bytes_per_step=step_bytes),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "peak_source": f"{peak_src} (copy bandwidth)",
+                         "kernel": "decode_kernel<128, half, 1>"},
+            "clocks": clk.summary(),
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

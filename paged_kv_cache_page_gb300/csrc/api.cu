@@ -1,0 +1,441 @@
+// C ABI of libpagedattn.so: argument validation, tensor-map encoding, the
+// host half of the split-KV plan (capacities only -- lengths stay on the GPU),
+// and kernel launches.  No function here synchronises or allocates.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool mult8(int64_t s) { return s > 0 && (s % 8) == 0; }
+
+// Split-KV planning constants.  The host only fixes a cap on splits per
+// sequence from capacities; the GPU picks the actual counts from the lengths.
+constexpr int kSplitCapTargetCtas = 304;  // 152 SMs x 2 resident decode CTAs
+constexpr int kMinChunkPages = 8;         // each split streams >= 128 keys
+constexpr int kMaxSplits = 128;
+
+int plan_s_max(int B, int Hkv, int max_seqlen_k, int num_splits) {
+  const int max_pages = std::max(1, (max_seqlen_k + kPage - 1) / kPage);
+  if (num_splits == 1) return 1;
+  if (num_splits > 1) return std::min(std::min(num_splits, kMaxSplits), max_pages);
+  if (B > kDecodeMaxSchedB) return 1;
+  if ((long long)B * Hkv >= 4LL * kSplitCapTargetCtas) return 1;
+  int s = (max_pages + kMinChunkPages - 1) / kMinChunkPages;
+  s = std::min(s, kSplitCapTargetCtas / std::max(1, Hkv) + 1);
+  s = std::min(s, kMaxSplits);
+  return std::max(1, s);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct SplitWorkspace {
+  size_t off_nsplit, off_lse, off_o, total;
+};
+
+SplitWorkspace split_workspace_layout(int B, long long rows, int Hq, int D, int s_max) {
+  SplitWorkspace w{};
+  if (s_max <= 1) return w;
+  w.off_nsplit = 0;
+  w.off_lse = align256((size_t)B * 4);
+  w.off_o = w.off_lse + align256((size_t)s_max * rows * Hq * 4);
+  w.total = w.off_o + align256((size_t)s_max * rows * Hq * D * 4);
+  return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int decode_resident_ctas(int D, int dtype, int rmax) {
+  static int cache[2][2][4] = {};
+  const int di = D == 128 ? 1 : 0, ri = rmax == 1 ? 0 : rmax == 2 ? 1 : rmax == 4 ? 2 : 3;
+  int& c = cache[di][dtype][ri];
+  if (c == 0) {
+    const int per_sm = std::max(1, decode_ctas_per_sm(D, dtype, rmax));
+    c = per_sm * num_sms();
+  }
+  return c;
+}
+
+int check_cache(const pa_tensor4& t, const char* name) {
+  if (t.ptr == nullptr) return fail(PA_ERR_INVALID_ARG, "%s.ptr is NULL", name);
+  if (!aligned16(t.ptr)) return fail(PA_ERR_INVALID_ARG, "%s.ptr must be 16-byte aligned", name);
+  if (!mult8(t.stride_b) || !mult8(t.stride_t) || !mult8(t.stride_h))
+    return fail(PA_ERR_INVALID_ARG,
+                "%s strides must be positive multiples of 8 elements (got %lld, %lld, %lld)", name,
+                (long long)t.stride_b, (long long)t.stride_t, (long long)t.stride_h);
+  return PA_OK;
+}
+
+int check_common(int dtype, int D, int Hq, int Hkv) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", D);
+  if (Hq < 1 || Hkv < 1) return fail(PA_ERR_INVALID_ARG, "head counts must be >= 1");
+  if (Hq % Hkv != 0) return fail(PA_ERR_UNSUPPORTED, "Hq %d not a multiple of Hkv %d", Hq, Hkv);
+  return PA_OK;
+}
+
+int rows_template(int rows) {
+  return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+bool encode_cache_map(CUtensorMap* map, const void* base, int dtype, int D, int Hkv, int64_t dim2,
+                      int64_t dim3, int64_t stride_h, int64_t stride_t, int64_t stride_b,
+                      int box_d, int box_rows, bool swizzle128) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  (void)dtype;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)dim2, (cuuint64_t)dim3};
+  const cuuint64_t strides[3] = {(cuuint64_t)stride_h * 2, (cuuint64_t)stride_t * 2,
+                                 (cuuint64_t)stride_b * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+PA_API const char* pa_last_error_string(void) { return g_last_error.c_str(); }
+
+PA_API int pa_version(void) { return 100; }
+
+PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                        const void* v_new, const int32_t* cache_seqlens,
+                        const int32_t* block_table, int64_t bt_stride, int max_pages, int B,
+                        int Lnew, int Hkv, int D, int64_t cache_extent, int dtype,
+                        int32_t* err_word, pa_stream_t stream) {
+  int rc = check_common(dtype, D, Hkv, Hkv);
+  if (rc) return rc;
+  if (B < 0 || Lnew < 0) return fail(PA_ERR_INVALID_ARG, "negative B or Lnew");
+  if (B == 0 || Lnew == 0) return PA_OK;
+  if ((rc = check_cache(k_cache, "k_cache")) || (rc = check_cache(v_cache, "v_cache"))) return rc;
+  if (k_new == nullptr || v_new == nullptr || cache_seqlens == nullptr)
+    return fail(PA_ERR_INVALID_ARG, "k_new, v_new and cache_seqlens must be non-NULL");
+  if (!aligned16(k_new) || !aligned16(v_new))
+    return fail(PA_ERR_INVALID_ARG, "k_new/v_new must be 16-byte aligned");
+  if (cache_extent < 1) return fail(PA_ERR_INVALID_ARG, "cache_extent must be >= 1");
+  if (block_table != nullptr && (max_pages < 1 || bt_stride < max_pages))
+    return fail(PA_ERR_INVALID_ARG, "block table needs max_pages >= 1 and bt_stride >= max_pages");
+  AppendParams p{};
+  p.k_cache = k_cache.ptr;
+  p.v_cache = v_cache.ptr;
+  p.k_sb = k_cache.stride_b; p.k_st = k_cache.stride_t; p.k_sh = k_cache.stride_h;
+  p.v_sb = v_cache.stride_b; p.v_st = v_cache.stride_t; p.v_sh = v_cache.stride_h;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.cache_seqlens = cache_seqlens;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.max_pages = max_pages;
+  p.extent = cache_extent;
+  p.B = B; p.Lnew = Lnew; p.Hkv = Hkv; p.D = D;
+  p.err = err_word;
+  const cudaError_t e = launch_append(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PA_OK;
+}
+
+PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int D,
+                                            int max_seqlen_k, int num_splits) {
+  if (B <= 0 || Lq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
+  const int rows = Lq * (Hq / Hkv);
+  if (rows > kDecodeMaxRows) return 0;  // tensor-core path needs no workspace
+  const int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
+  return split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max).total;
+}
+
+PA_API size_t pa_fwd_varlen_workspace_size(int B, int total_q, int max_seqlen_q, int Hq,
+                                           int Hkv, int D, int max_seqlen_k) {
+  if (B <= 0 || total_q <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
+  (void)max_seqlen_q;
+  const int s_max = plan_s_max(std::min(B, kDecodeMaxSchedB), Hkv, max_seqlen_k, 0);
+  return split_workspace_layout(B, total_q, Hq, D, s_max).total;
+}
+
+PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                          pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                          const void* v_new, int Lnew, const int32_t* cache_seqlens,
+                          const int32_t* block_table, int64_t bt_stride, int max_pages, int B,
+                          int Lq, int Hq, int Hkv, int D, int64_t cache_extent, int max_seqlen_k,
+                          float scale, int causal, int num_splits, void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, int32_t* err_word, int dtype,
+                          pa_stream_t stream) {
+  int rc = check_common(dtype, D, Hq, Hkv);
+  if (rc) return rc;
+  if (B < 0 || Lq < 0 || Lnew < 0 || max_seqlen_k < 0 || num_splits < 0)
+    return fail(PA_ERR_INVALID_ARG, "negative size argument");
+  if (B == 0) return PA_OK;
+  if ((rc = check_cache(k_cache, "k_cache")) || (rc = check_cache(v_cache, "v_cache"))) return rc;
+  if (cache_seqlens == nullptr) return fail(PA_ERR_INVALID_ARG, "cache_seqlens is NULL");
+  if (Lnew > 0 && (k_new == nullptr || v_new == nullptr || !aligned16(k_new) || !aligned16(v_new)))
+    return fail(PA_ERR_INVALID_ARG, "Lnew > 0 needs 16-byte aligned k_new and v_new");
+  if (cache_extent < 1) return fail(PA_ERR_INVALID_ARG, "cache_extent must be >= 1");
+  if (block_table != nullptr && (max_pages < 1 || bt_stride < max_pages))
+    return fail(PA_ERR_INVALID_ARG, "block table needs max_pages >= 1 and bt_stride >= max_pages");
+  if (Lq == 0) {
+    if (Lnew == 0) return PA_OK;
+    return pa_append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table, bt_stride,
+                        max_pages, B, Lnew, Hkv, D, cache_extent, dtype, err_word, stream);
+  }
+  if (q == nullptr || out == nullptr) return fail(PA_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(out))
+    return fail(PA_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (!mult8(q_sh) || !mult8(q_st) || !mult8(q_sb))
+    return fail(PA_ERR_INVALID_ARG, "q strides must be positive multiples of 8 elements");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(PA_ERR_INVALID_ARG, "scale must be finite and > 0");
+
+  const int G = Hq / Hkv;
+  const int rows = Lq * G;
+  if (rows > kDecodeMaxRows)
+    return fail(PA_ERR_UNSUPPORTED, "query block of %d rows per kv head: prefill path", rows);
+
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int rmax = rows_template(rows);
+  const int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
+  const SplitWorkspace ws = split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max);
+  if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
+    return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
+                workspace_bytes);
+
+  CUtensorMap tmk, tmv;
+  const bool paged = block_table != nullptr;
+  const int64_t dim2 = paged ? kPage : cache_extent;
+  const int64_t dim3 = paged ? cache_extent : B;
+  if (!encode_cache_map(&tmk, k_cache.ptr, dtype, D, Hkv, dim2, dim3, k_cache.stride_h,
+                        k_cache.stride_t, k_cache.stride_b, D, kPage, false) ||
+      !encode_cache_map(&tmv, v_cache.ptr, dtype, D, Hkv, dim2, dim3, v_cache.stride_h,
+                        v_cache.stride_t, v_cache.stride_b, D, kPage, false))
+    return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for the cache views");
+
+  DecodeParams p{};
+  p.q = q;
+  p.q_sb = q_sb; p.q_st = q_st; p.q_sh = q_sh;
+  p.out = out;
+  p.lse = lse;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.Lnew = Lnew;
+  p.k_cache = k_cache.ptr;
+  p.v_cache = v_cache.ptr;
+  p.k_sb = k_cache.stride_b; p.k_st = k_cache.stride_t; p.k_sh = k_cache.stride_h;
+  p.v_sb = v_cache.stride_b; p.v_st = v_cache.stride_t; p.v_sh = v_cache.stride_h;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.max_pages = paged ? max_pages : 0;
+  p.extent = cache_extent;
+  p.cache_seqlens = cache_seqlens;
+  p.cu_seqlens_q = nullptr;
+  p.seqlens_k = nullptr;
+  p.B = B; p.Lq = Lq; p.Hq = Hq; p.Hkv = Hkv; p.G = G;
+  p.max_seqlen_k = max_seqlen_k;
+  p.total_q = 0;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.s_max = s_max;
+  const int resident = decode_resident_ctas(D, dtype, rmax);
+  p.target_ctas = num_splits > 0 ? (1 << 30) : resident;
+  p.grid_ctas = resident;
+  p.min_chunk_pages = num_splits > 0 ? 1 : kMinChunkPages;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(workspace);
+  p.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
+  p.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
+  p.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
+  p.err = err_word;
+
+  cudaError_t e = launch_decode(p, tmk, tmv, D, dtype, rmax, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (s_max > 1) {
+    CombineParams c{};
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.nsplit = p.nsplit;
+    c.S = s_max;
+    c.B = B; c.Lq = Lq; c.Hq = Hq;
+    c.cu_seqlens_q = nullptr;
+    c.total_q = 0;
+    c.out = out;
+    c.lse = lse;
+    e = launch_combine(c, D, dtype, B * Lq, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return PA_OK;
+}
+
+PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_tensor4 k_cache,
+                                 pa_tensor4 v_cache, const int32_t* cu_seqlens_q,
+                                 const int32_t* seqlens_k, const int32_t* block_table,
+                                 int64_t bt_stride, int max_pages, int B, int total_q,
+                                 int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
+                                 int64_t num_pages, float scale, int causal, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t* err_word, int dtype, pa_stream_t stream) {
+  int rc = check_common(dtype, D, Hq, Hkv);
+  if (rc) return rc;
+  if (B < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(PA_ERR_INVALID_ARG, "negative size argument");
+  if (B == 0 || total_q == 0) return PA_OK;
+  if ((rc = check_cache(k_cache, "k_cache")) || (rc = check_cache(v_cache, "v_cache"))) return rc;
+  if (q == nullptr || out == nullptr || cu_seqlens_q == nullptr || seqlens_k == nullptr ||
+      block_table == nullptr)
+    return fail(PA_ERR_INVALID_ARG, "q, out, cu_seqlens_q, seqlens_k, block_table must be non-NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(PA_ERR_INVALID_ARG, "q/out 16-byte alignment");
+  if (!mult8(q_st) || !mult8(q_sh)) return fail(PA_ERR_INVALID_ARG, "q strides multiples of 8");
+  if (max_pages < 1 || bt_stride < max_pages || num_pages < 1)
+    return fail(PA_ERR_INVALID_ARG, "block table / pool sizes");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale");
+  if (B > kDecodeMaxSchedB) return fail(PA_ERR_UNSUPPORTED, "more than %d sequences", kDecodeMaxSchedB);
+  const int G = Hq / Hkv;
+  if (max_seqlen_q * G > kDecodeMaxRows)
+    return fail(PA_ERR_UNSUPPORTED, "prefill sequences in the unified launch");
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int rmax = kDecodeMaxRows;
+  const int s_max = plan_s_max(B, Hkv, max_seqlen_k, 0);
+  const SplitWorkspace ws = split_workspace_layout(B, total_q, Hq, D, s_max);
+  if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
+    return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
+                workspace_bytes);
+  CUtensorMap tmk, tmv;
+  if (!encode_cache_map(&tmk, k_cache.ptr, dtype, D, Hkv, kPage, num_pages, k_cache.stride_h,
+                        k_cache.stride_t, k_cache.stride_b, D, kPage, false) ||
+      !encode_cache_map(&tmv, v_cache.ptr, dtype, D, Hkv, kPage, num_pages, v_cache.stride_h,
+                        v_cache.stride_t, v_cache.stride_b, D, kPage, false))
+    return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for the cache views");
+  DecodeParams p{};
+  p.q = q;
+  p.q_sb = 0; p.q_st = q_st; p.q_sh = q_sh;
+  p.out = out;
+  p.lse = lse;
+  p.k_cache = k_cache.ptr;
+  p.v_cache = v_cache.ptr;
+  p.k_sb = k_cache.stride_b; p.k_st = k_cache.stride_t; p.k_sh = k_cache.stride_h;
+  p.v_sb = v_cache.stride_b; p.v_st = v_cache.stride_t; p.v_sh = v_cache.stride_h;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.max_pages = max_pages;
+  p.extent = num_pages;
+  p.cu_seqlens_q = cu_seqlens_q;
+  p.seqlens_k = seqlens_k;
+  p.B = B; p.Lq = 0; p.Hq = Hq; p.Hkv = Hkv; p.G = G;
+  p.max_seqlen_k = max_seqlen_k;
+  p.total_q = total_q;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.s_max = s_max;
+  const int resident = decode_resident_ctas(D, dtype, rmax);
+  p.target_ctas = resident;
+  p.grid_ctas = resident;
+  p.min_chunk_pages = kMinChunkPages;
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(workspace);
+  p.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
+  p.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
+  p.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
+  p.err = err_word;
+  cudaError_t e = launch_decode(p, tmk, tmv, D, dtype, rmax, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (s_max > 1) {
+    CombineParams c{};
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.nsplit = p.nsplit;
+    c.S = s_max;
+    c.B = B; c.Lq = 0; c.Hq = Hq;
+    c.cu_seqlens_q = cu_seqlens_q;
+    c.total_q = total_q;
+    c.out = out;
+    c.lse = lse;
+    e = launch_combine(c, D, dtype, total_q, st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return PA_OK;
+}
+
+PA_API int pa_split_combine(const float* o_partial, const float* lse_partial,
+                            const int32_t* splits_per_seq, int S, int B, int Lq, int Hq, int D,
+                            void* out, float* lse, int dtype, pa_stream_t stream) {
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (D != 64 && D != 128) return fail(PA_ERR_UNSUPPORTED, "head_dim %d", D);
+  if (S < 1 || B < 0 || Lq < 0 || Hq < 1) return fail(PA_ERR_INVALID_ARG, "sizes");
+  if (B == 0 || Lq == 0) return PA_OK;
+  if (o_partial == nullptr || lse_partial == nullptr || out == nullptr)
+    return fail(PA_ERR_INVALID_ARG, "o_partial, lse_partial and out must be non-NULL");
+  if (!aligned16(o_partial) || !aligned16(out))
+    return fail(PA_ERR_INVALID_ARG, "o_partial/out must be 16-byte aligned");
+  CombineParams c{};
+  c.o_part = o_partial;
+  c.lse_part = lse_partial;
+  c.nsplit = splits_per_seq;
+  c.S = S;
+  c.B = B; c.Lq = Lq; c.Hq = Hq;
+  c.cu_seqlens_q = nullptr;
+  c.total_q = 0;
+  c.out = out;
+  c.lse = lse;
+  const cudaError_t e =
+      launch_combine(c, D, dtype, B * Lq, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return PA_OK;
+}
+
+}  // extern "C"

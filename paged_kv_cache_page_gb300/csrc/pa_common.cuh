@@ -1,0 +1,247 @@
+// Device-side building blocks shared by the paged-attention kernels (sm_103a):
+// mbarrier pipeline primitives with bounded waits, TMA tensor loads, fast
+// exp2/log2, element-type traits, error reporting and the device split-KV
+// schedule.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedattn.h"
+#include "pa_internal.h"
+
+namespace pa {
+// A pipeline wait that has not completed after this long is treated as a
+// failure: the kernel records PA_DEVERR_TIMEOUT and finishes without waiting.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------- element types
+template <typename T> struct Elem;
+template <> struct Elem<__half> {
+  using T2 = __half2;
+  static __device__ __forceinline__ float2 to_f2(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+  }
+  static __device__ __forceinline__ uint32_t from_f2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ __half from_f(float a) { return __float2half_rn(a); }
+};
+template <> struct Elem<__nv_bfloat16> {
+  using T2 = __nv_bfloat162;
+  static __device__ __forceinline__ float2 to_f2(uint32_t u) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(h);
+  }
+  static __device__ __forceinline__ uint32_t from_f2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float a) { return __float2bfloat16_rn(a); }
+};
+
+// ---------------------------------------------------------------- math
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// ---------------------------------------------------------------- errors
+__device__ __forceinline__ void report(int32_t* err, int code, int b, int value) {
+  if (err == nullptr) return;
+  if (atomicCAS(err, 0, code) == 0) {
+    err[1] = b;
+    err[2] = value;
+  }
+}
+
+// ---------------------------------------------------------------- timers
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of parity `parity` to complete.  Returns false
+// (and never blocks longer than kWaitTimeoutNs) if it does not.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+  }
+  return true;
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA / tensor core) accesses of the same locations.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// 4-D tiled bulk tensor load global -> shared, completion signalled on `bar`
+// as transaction bytes.  c0 is the innermost (head_dim) coordinate and is
+// always 0 or a multiple of 64 elements here, which keeps it 16-byte aligned.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---------------------------------------------------------------- page resolution
+// Where logical page `lp` of sequence `b` lives, as TMA coordinates
+// (row coordinate c2, page-or-sequence coordinate c3) and as an element
+// offset of its first token slot for head 0.  The page is resolved absolutely
+// for every iteration (never by a delta from the previous page), and the
+// table is never indexed at or beyond `max_pages`.
+struct PageRef {
+  int c2, c3;
+  int64_t elem_off;  // offset of slot 0, head 0 (element units) in the K cache view
+  bool ok;           // false: entry out of range (reads use page 0, writes skipped)
+};
+
+struct CacheGeom {
+  const int32_t* block_table;  // nullptr: contiguous cache
+  int64_t bt_stride;
+  int max_pages;      // table width (paged)
+  int64_t extent;     // pages in pool (paged) or tokens per sequence (contiguous)
+  int64_t sb, st;     // element strides of the K cache (V uses its own strides)
+};
+
+__device__ __forceinline__ PageRef resolve_page(const CacheGeom& g, int b, int lp) {
+  PageRef r;
+  if (g.block_table != nullptr) {
+    int phys = 0;
+    bool ok = lp >= 0 && lp < g.max_pages;
+    if (ok) phys = __ldg(g.block_table + (int64_t)b * g.bt_stride + lp);
+    ok = ok && phys >= 0 && (int64_t)phys < g.extent;
+    if (!ok) phys = 0;
+    r.c2 = 0;
+    r.c3 = phys;
+    r.elem_off = (int64_t)phys * g.sb;
+    r.ok = ok;
+  } else {
+    // Rows past the capacity in the last box are zero-filled by the TMA unit
+    // and never written; only the box start must lie inside the cache.
+    const int64_t row = (int64_t)lp * kPage;
+    const bool ok = lp >= 0 && row < g.extent;
+    r.c2 = ok ? (int)row : 0;
+    r.c3 = b;
+    r.elem_off = (int64_t)b * g.sb + (ok ? row : 0) * g.st;
+    r.ok = ok;
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------- split-KV schedule
+// Device-side choice of the number of KV splits per sequence (replacing a
+// host heuristic that would need the lengths on the CPU).  All CTAs of a
+// launch evaluate the same function of the same inputs, so they agree.
+//
+//   pages_b      = ceil(Lk_b / 16)
+//   total        = Hkv * sum_b pages_b       (page-heads of K/V to stream)
+//   chunk        = max(min_chunk, ceil(total / slots)), rounded up to 4 pages
+//   n_b          = clamp(ceil(pages_b / chunk), 1, s_max)
+//   per_b        = ceil(pages_b / n_b) rounded up to 4 pages; n_b = ceil(pages_b / per_b)
+// where slots = max(target_ctas - B*Hkv, target_ctas / 2) keeps the number
+// of work items near one wave of resident CTAs.
+struct SplitSched {
+  int s_max;
+  int target_ctas;
+  int min_chunk_pages;
+};
+
+__device__ __forceinline__ int round_up4(int x) { return (x + 3) & ~3; }
+
+__device__ __forceinline__ int split_chunk_pages(const SplitSched& s, long long total_page_heads,
+                                                 int B, int Hkv) {
+  long long slots = (long long)s.target_ctas - (long long)B * Hkv;
+  if (slots < s.target_ctas / 2) slots = s.target_ctas / 2;
+  if (slots < 1) slots = 1;
+  long long c = (total_page_heads + slots - 1) / slots;
+  if (c < s.min_chunk_pages) c = s.min_chunk_pages;
+  if (c > (1 << 28)) c = 1 << 28;
+  return round_up4((int)c);
+}
+
+// Pages per split for a sequence of `pages` pages; writes the split count.
+__device__ __forceinline__ int split_pages_per(const SplitSched& s, int pages, int chunk,
+                                               int* n_out) {
+  if (s.s_max <= 1 || pages <= 0) {
+    *n_out = 1;
+    return pages > 0 ? pages : 0;
+  }
+  int n = (pages + chunk - 1) / chunk;
+  if (n < 1) n = 1;
+  if (n > s.s_max) n = s.s_max;
+  int per = round_up4((pages + n - 1) / n);
+  n = (pages + per - 1) / per;
+  *n_out = n;
+  return per;
+}
+
+}  // namespace pa

@@ -1,0 +1,95 @@
+// Internal (non-exported) declarations shared by the host-side API and the
+// kernel translation units of libpagedattn.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+constexpr int kPage = 16;  // tokens per page
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Parameters of the split-KV decode path (also the decode part of the unified
+// varlen launch).  Rows of one work item are the Lq_b * G query rows that
+// share one kv head of one sequence.
+struct DecodeParams {
+  const void* q;
+  int64_t q_sb, q_st, q_sh;  // element strides (varlen: q_sb unused, rows by q_st)
+  void* out;                 // kvcache: [B, Lq, Hq, D]; varlen: [total_q, Hq, D]
+  float* lse;                // kvcache: [B, Hq, Lq]; varlen: [Hq, total_q]; may be null
+  const void* k_new;         // [B, Lnew, Hkv, D] or null
+  const void* v_new;
+  int Lnew;
+  void* k_cache;
+  void* v_cache;
+  int64_t k_sb, k_st, k_sh, v_sb, v_st, v_sh;
+  const int32_t* block_table;  // null: contiguous cache
+  int64_t bt_stride;
+  int max_pages;
+  int64_t extent;  // pages in pool, or tokens per sequence (contiguous)
+  const int32_t* cache_seqlens;  // kvcache mode
+  const int32_t* cu_seqlens_q;   // varlen mode (non-null selects it)
+  const int32_t* seqlens_k;      // varlen mode
+  int B, Lq, Hq, Hkv, G, max_seqlen_k, total_q;
+  float scale_log2;  // softmax scale * log2(e)
+  int causal;
+  int s_max, target_ctas, min_chunk_pages;
+  int grid_ctas;     // persistent CTAs launched (resident capacity)
+  float* o_part;     // [s_max, NR, Hq, D] (NR = B*Lq or total_q)
+  float* lse_part;   // [s_max, NR, Hq]
+  int32_t* nsplit;   // [B]: splits to combine (0: final output already written)
+  int32_t* err;
+};
+
+struct CombineParams {
+  const float* o_part;
+  const float* lse_part;
+  const int32_t* nsplit;  // null: all S splits valid
+  int S, B, Lq, Hq;
+  const int32_t* cu_seqlens_q;  // non-null: varlen row addressing
+  int total_q;
+  void* out;
+  float* lse;
+};
+
+struct AppendParams {
+  void* k_cache;
+  void* v_cache;
+  int64_t k_sb, k_st, k_sh, v_sb, v_st, v_sh;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* cache_seqlens;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_pages;
+  int64_t extent;
+  int B, Lnew, Hkv, D;
+  int32_t* err;
+};
+
+// Launchers (each defined in the .cu file that holds its kernel).  They
+// return a cudaError_t from the launch.
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+cudaError_t launch_combine(const CombineParams& p, int D, int dtype, int rows_total,
+                           cudaStream_t st);
+// Decode: `rmax` in {1,2,4,8}.  tmk/tmv are 4-D tensor maps of the caches
+// with box {D, 1, 16, 1}.
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          int D, int dtype, int rmax, cudaStream_t st);
+// Resident CTAs per SM of the decode kernel for this configuration (0 on error).
+int decode_ctas_per_sm(int D, int dtype, int rmax);
+constexpr int kDecodeMaxRows = 8;
+constexpr int kDecodeMaxSchedB = 512;
+
+// Host helpers (api.cu).
+int num_sms();
+bool encode_cache_map(CUtensorMap* map, const void* base, int dtype, int D, int Hkv, int64_t dim2,
+                      int64_t dim3, int64_t stride_h, int64_t stride_t, int64_t stride_b,
+                      int box_d, int box_rows, bool swizzle128);
+
+}  // namespace pa
