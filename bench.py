@@ -106,6 +106,9 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0:  # first sample before timing
+                time.sleep(0.02)
         except Exception:
             self.proc = None
         return self
@@ -186,22 +189,25 @@ def host_sample(w, seqs):
     return out
 
 
-def cpu_baseline(w, budget_s=10.0):
-    import torch
-
+def cpu_baseline(w, budget_s=10.0, max_seqs=8):
+    """Oracle throughput on a bounded sample: up to `max_seqs` sequences of the
+    workload (held on the host in float64), passed repeatedly until about
+    `budget_s` seconds of CPU work have been timed."""
     lnew = WORKLOAD["lnew"]
-    probe = [0]
-    hs = host_sample(w, probe)
-    rate, dt = cpu_oracle_rate(hs, probe, lnew)
-    n = max(1, min(64, int(budget_s / max(dt, 1e-3))))
-    seqs = list(range(n))
+    seqs = list(range(min(max_seqs, w["q"].shape[0])))
     hs = host_sample(w, seqs)
-    rate, dt = cpu_oracle_rate(hs, seqs, lnew)
-    del torch
+    total_bytes, total_s, passes = 0.0, 0.0, 0
+    while total_s < budget_s and passes < 1000:
+        rate, dt = cpu_oracle_rate(hs, seqs, lnew)
+        total_bytes += rate * dt * 1e9
+        total_s += dt
+        passes += 1
+    rate = total_bytes / total_s / 1e9
     return {"value": round(rate, 3), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} of {WORKLOAD['batch']} sequences (ctx {WORKLOAD['ctx']}, 32x128 "
-                      f"heads) through the float64 numpy oracle, {dt:.1f} s; cores = host "
-                      f"threads available to its BLAS"}
+            "sample": f"{len(seqs)} of {WORKLOAD['batch']} sequences (ctx {WORKLOAD['ctx']}, "
+                      f"32x128 heads, fp16 values widened to float64) through the numpy oracle, "
+                      f"{passes} passes, {total_s:.1f} s; cores = host threads available to "
+                      f"its BLAS"}
 
 
 def run_reference(args, rank, world):
@@ -254,11 +260,15 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=WORKLOAD["batch"],
+                    help="smaller batches are for profiling runs only")
+    ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     args = ap.parse_args()
+    WORKLOAD["batch"], WORKLOAD["ctx"] = args.batch, args.ctx
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
 
