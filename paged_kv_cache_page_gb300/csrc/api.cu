@@ -42,9 +42,10 @@ constexpr int kMaxSplits = 128;
 
 int plan_s_max(int B, int Hkv, int max_seqlen_k, int num_splits) {
   const int max_pages = std::max(1, (max_seqlen_k + kPage - 1) / kPage);
-  if (num_splits == 1) return 1;
+  // The device schedule keeps one prefix entry per sequence in shared memory;
+  // batches beyond that table run unsplit (they have parallelism to spare).
+  if (num_splits == 1 || B > kDecodeMaxSchedB) return 1;
   if (num_splits > 1) return std::min(std::min(num_splits, kMaxSplits), max_pages);
-  if (B > kDecodeMaxSchedB) return 1;
   if ((long long)B * Hkv >= 4LL * kSplitCapTargetCtas) return 1;
   int s = (max_pages + kMinChunkPages - 1) / kMinChunkPages;
   s = std::min(s, kSplitCapTargetCtas / std::max(1, Hkv) + 1);

@@ -101,3 +101,10 @@ def test_workspace_sizes(lib):
     assert n4 >= 4 * 2 * 4 * 65 * 4
     # the tensor-core prefill path takes no workspace
     assert lib.pa_fwd_kvcache_workspace_size(4, 170, 32, 32, 128, 1024, 0) == 0
+
+
+def test_split_cap_respects_schedule_table(lib):
+    # more sequences than the device schedule's prefix table: never split,
+    # even when splits are requested
+    assert lib.pa_fwd_kvcache_workspace_size(513, 1, 8, 8, 128, 4096, 4) == 0
+    assert lib.pa_fwd_kvcache_workspace_size(512, 1, 8, 8, 128, 4096, 4) > 0
