@@ -159,6 +159,39 @@ PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int 
                                             int max_seqlen_k, int num_splits);
 
 /*
+ * pa_fwd_kvcache_noalloc -- pa_fwd_kvcache for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: this is a library-usage entry
+ * point, not part of the attention method.)
+ *
+ * Some callers cannot call cudaMalloc: code running inside another library's
+ * allocator or stream callback, serving processes whose device memory pool is
+ * owned and capped by the framework, or latency paths that must never reach
+ * the driver's allocator.  They can pass inputs and outputs but not the
+ * split-KV scratch that pa_fwd_kvcache takes as `workspace`.  This variant
+ * takes the same arguments minus the workspace and uses a fixed scratch array
+ * of PA_NOALLOC_SCRATCH_BYTES that every GPU loading the library reserves
+ * until the process exits.  It calls no allocating routine.
+ *
+ *   - Sizes whose split scratch (pa_fwd_kvcache_workspace_size) exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES are rejected with PA_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the array, which keeps the last call's contents; no
+ *     entry needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     (other streams, other threads) race on it: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (8 << 20)
+PA_API int pa_fwd_kvcache_noalloc(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                                  pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                                  const void* v_new, int Lnew, const int32_t* cache_seqlens,
+                                  const int32_t* block_table, int64_t bt_stride, int max_pages,
+                                  int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
+                                  int max_seqlen_k, float scale, int causal, int num_splits,
+                                  void* out, float* lse, int32_t* err_word, int dtype,
+                                  pa_stream_t stream);
+
+/*
  * pa_fwd_varlen_unified -- one launch for a mixed batch of chunked-prefill
  * and decode sequences over a paged cache (vLLM #6052 "Unify the kernel used
  * in flash attention backend": a single varlen kernel for prefill, decode and

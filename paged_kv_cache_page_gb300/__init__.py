@@ -31,6 +31,7 @@ PA_DEVERR_PAGE_OOB = 1
 PA_DEVERR_LENGTH = 2
 PA_DEVERR_TIMEOUT = 3
 PAGE_SIZE = 16
+PA_NOALLOC_SCRATCH_BYTES = 8 << 20  # fixed split scratch of pa_fwd_kvcache_noalloc
 
 _DTYPE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
@@ -57,6 +58,9 @@ _SIGNATURES = {
                               _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
                               _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
     "pa_fwd_kvcache_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_fwd_kvcache_noalloc": (_i32, [_vp, _i64, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp,
+                                      _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32,
+                                      _i64, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _i32, _vp]),
     "pa_fwd_varlen_unified": (_i32, [_vp, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp, _vp,
                                      _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
                                      _f32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
@@ -184,6 +188,40 @@ def pa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, k=None,
                               max_seqlen_k, float(scale), int(bool(causal)), int(num_splits),
                               _ptr(out), _ptr(lse), _ptr(workspace), ws_len, _ptr(err),
                               _dtype(q), _stream(q)))
+    return out, lse
+
+
+def pa_fwd_kvcache_noalloc(q, k_cache, v_cache, cache_seqlens, out, block_table=None, k=None,
+                           v=None, lse=None, scale=None, causal=False, num_splits=0, err=None,
+                           max_seqlen_k=None):
+    """pa_fwd_kvcache for callers that cannot allocate device memory.
+
+    The caller passes every tensor, including ``out`` (and optionally ``lse``);
+    this wrapper allocates nothing and the library uses its own fixed split
+    scratch (``PA_NOALLOC_SCRATCH_BYTES``).  Calls that could overlap on the GPU
+    must be serialised by the caller because they share that scratch.
+    """
+    lib = load_library()
+    _cuda(q, k_cache, v_cache, cache_seqlens, block_table, k, v, out, lse)
+    B, lq, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    lnew = 0 if k is None else k.shape[1]
+    if block_table is not None:
+        extent, max_pages, bt_stride = k_cache.shape[0], block_table.shape[1], block_table.stride(0)
+        cap = max_pages * PAGE_SIZE
+    else:
+        extent, max_pages, bt_stride = k_cache.shape[1], 0, 0
+        cap = extent
+    if max_seqlen_k is None:
+        max_seqlen_k = cap
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(lib.pa_fwd_kvcache_noalloc(_ptr(q), q.stride(0), q.stride(1), q.stride(2),
+                                      _t4(k_cache), _t4(v_cache), _ptr(k), _ptr(v), lnew,
+                                      _ptr(cache_seqlens), _ptr(block_table), bt_stride,
+                                      max_pages, B, lq, hq, hkv, d, extent, max_seqlen_k,
+                                      float(scale), int(bool(causal)), int(num_splits),
+                                      _ptr(out), _ptr(lse), _ptr(err), _dtype(q), _stream(q)))
     return out, lse
 
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libpagedattn.so"
-SOURCES = ["api.cu", "append.cu", "decode.cu", "combine.cu"]
+SOURCES = ["api.cu", "append.cu", "decode.cu", "combine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

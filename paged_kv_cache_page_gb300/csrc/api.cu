@@ -118,6 +118,16 @@ int rows_template(int rows) {
 
 }  // namespace
 
+int set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
 int num_sms() {
   static int sms[64] = {};
   int dev = 0;
