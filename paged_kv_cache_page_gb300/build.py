@@ -1,4 +1,5 @@
-"""Build libpagedattn.so in-tree with nvcc for sm_103a.
+"""Build libpagedattn.so (and the test-only libpa_selftest.so) in-tree with
+nvcc for sm_103a.
 
 Each translation unit is compiled in parallel, then linked into a shared
 library with the CUDA runtime linked statically (no libcuda dependency at load
@@ -18,6 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libpagedattn.so"
 SOURCES = ["api.cu", "append.cu", "decode.cu", "combine.cu", "noalloc.cu"]
+# Encoding self-test of the tensor-core operand layouts: test infrastructure,
+# kept out of the product library.
+SELFTEST_LIB = "libpa_selftest.so"
+SELFTEST_SOURCES = ["selftest_tcgen05.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,8 +33,8 @@ def nvcc_path():
     raise RuntimeError("nvcc not found")
 
 
-def lib_path():
-    return os.path.join(OUT_DIR, LIB_NAME)
+def lib_path(name=LIB_NAME):
+    return os.path.join(OUT_DIR, name)
 
 
 def _flags(extra=()):
@@ -54,34 +59,41 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _link(lib, objs):
+    tmp = lib + ".tmp"
+    cmd = [nvcc_path(), "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+
+
 def build(force=False, verbose=False, extra=()):
-    """Compile (if needed) and return the path of libpagedattn.so."""
+    """Compile (if needed) both libraries; return the path of libpagedattn.so."""
     os.makedirs(OUT_DIR, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(ROOT, "include", "pagedattn.h"))
-    objs, jobs = [], []
-    for src in SOURCES:
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
-        objs.append(obj)
-        if force or verbose or _stale(obj, [os.path.join(CSRC, src)] + headers):
-            jobs.append((src, obj))
+    targets = [(lib_path(LIB_NAME), SOURCES), (lib_path(SELFTEST_LIB), SELFTEST_SOURCES)]
+    jobs, objs_of = [], {}
+    for lib, sources in targets:
+        objs_of[lib] = []
+        for src in sources:
+            obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+            objs_of[lib].append(obj)
+            if force or verbose or _stale(obj, [os.path.join(CSRC, src)] + headers):
+                jobs.append((src, obj))
     logs = []
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             futs = [ex.submit(_compile, s, o, extra, verbose) for s, o in jobs]
             for f in futs:
                 logs.append(f.result())
-    lib = lib_path()
-    if force or jobs or _stale(lib, objs):
-        tmp = lib + ".tmp"
-        cmd = [nvcc_path(), "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, lib)
+    for lib, objs in objs_of.items():
+        if force or _stale(lib, objs):
+            _link(lib, objs)
     if verbose:
         print("\n".join(logs))
-    return lib
+    return lib_path(LIB_NAME)
 
 
 if __name__ == "__main__":
