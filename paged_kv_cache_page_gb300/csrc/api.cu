@@ -11,6 +11,7 @@
 #include <string>
 
 #include "pa_internal.h"
+#include "pa_prefill.h"
 
 namespace pa {
 namespace {
@@ -259,10 +260,45 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
 
   const int G = Hq / Hkv;
   const int rows = Lq * G;
-  if (rows > kDecodeMaxRows)
-    return fail(PA_ERR_UNSUPPORTED, "query block of %d rows per kv head: prefill path", rows);
-
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (rows > kDecodeMaxRows) {
+    // Tensor-core prefill: the new tokens are appended first (same stream),
+    // then every key is read from the cache.
+    if (Lnew > 0) {
+      rc = pa_append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table, bt_stride,
+                        max_pages, B, Lnew, Hkv, D, cache_extent, dtype, err_word, stream);
+      if (rc) return rc;
+    }
+    const bool paged_p = block_table != nullptr;
+    CUtensorMap tq, tk, tv;
+    if (!encode_cache_map(&tq, q, dtype, D, Hq, Lq, B, q_sh, q_st, q_sb, 64, 128, true) ||
+        !encode_cache_map(&tk, k_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
+                          paged_p ? cache_extent : B, k_cache.stride_h, k_cache.stride_t,
+                          k_cache.stride_b, 64, kPage, true) ||
+        !encode_cache_map(&tv, v_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
+                          paged_p ? cache_extent : B, v_cache.stride_h, v_cache.stride_t,
+                          v_cache.stride_b, 64, kPage, true))
+      return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for q or the caches");
+    PrefillParams pp{};
+    pp.out = out;
+    pp.lse = lse;
+    pp.cache_seqlens = cache_seqlens;
+    pp.Lnew = Lnew;
+    pp.block_table = block_table;
+    pp.bt_stride = bt_stride;
+    pp.max_pages = paged_p ? max_pages : 0;
+    pp.extent = cache_extent;
+    pp.B = B; pp.Lq = Lq; pp.Hq = Hq; pp.Hkv = Hkv; pp.G = G;
+    pp.max_seqlen_k = max_seqlen_k;
+    pp.q_tiles = (Lq + 127) / 128;
+    pp.scale_log2 = scale * kLog2e;
+    pp.causal = causal ? 1 : 0;
+    pp.err = err_word;
+    const cudaError_t e = launch_prefill(pp, tq, tk, tv, D, dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return PA_OK;
+  }
+
   const int rmax = rows_template(rows);
   const int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
   const SplitWorkspace ws = split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max);
