@@ -60,6 +60,151 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
+def read_tensor_peak():
+    """Dense 16-bit tensor peak in TFLOP/s (fp16 and bf16 run at the same rate):
+    the burst figure for a kernel timed alone."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def attention_flops(q_lens, k_lens, heads, d, causal):
+    """4*D flops (QK^T and PV) per visible (query, key) pair, summed exactly."""
+    total = 0
+    for lq, lk in zip(q_lens, k_lens):
+        if causal:
+            pairs = sum(max(0, min(lk, i + lk - lq + 1)) for i in range(lq))
+        else:
+            pairs = lq * lk
+        total += pairs
+    return 4 * d * heads * total
+
+
+def time_calls(fn, steps, warmup, stream, graph=True):
+    """Device time per call in us.  With `graph`, `steps` calls are captured in
+    one CUDA graph and replayed, so host launch overhead does not show up as
+    idle device time for short kernels (the library never synchronises or
+    reads lengths on the host, so its calls capture as they are)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(steps):
+                    fn()
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    else:
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps * 1e3
+
+
+def secondary_measurements(dev, only=None):
+    """Other configurations of the path, each timed alone with CUDA events
+    (median-free mean over the timed calls, after warm-up)."""
+    import torch
+
+    import paged_kv_cache_page_gb300 as pa
+    from paged_kv_cache_page_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream(dev)
+    tpeak, tsrc = read_tensor_peak()
+    hpeak, hsrc = read_peaks()
+    res = {}
+    if only == "prefill" or only is None:
+        # causal prefill large enough for the tensor-core roofline to matter:
+        # 16 sequences x 4096 new tokens, 32 heads, D 128, fp16, appended in-call
+        w = wl.prefill_append(batch=16, lnew=4096, num_heads=32, head_dim=128, old_lo=0,
+                              old_hi=0, pool=16 * 256, dtype="f16", dist="normal", seed=1006,
+                              device=dev)
+        out = torch.empty_like(w["q"])
+        fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                       w["block_table"], k=w["k_new"], v=w["v_new"], causal=True,
+                                       out=out, return_lse=False)
+        us_append = time_calls(fn, 5 if only is None else 2, 2, stream)
+        # the same attention with the 4096 tokens already cached: the prefill
+        # kernel alone (one launch per call)
+        full = (w["cache_seqlens"] + 4096).contiguous()
+        fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], full,  # noqa: E731
+                                       w["block_table"], causal=True, out=out, return_lse=False)
+        us = time_calls(fn, 10 if only is None else 3, 3, stream)
+        fl = attention_flops([4096] * 16, [4096] * 16, 32, 128, True)
+        res["prefill_causal_16x4096"] = {
+            "us": round(us, 1), "tflops": round(fl / us / 1e6, 1),
+            "roofline": {"bound": "tensor", "achieved": round(fl / us / 1e6, 1), "peak": tpeak,
+                         "unit": "TFLOP/s", "frac": round(fl / us / 1e6 / tpeak, 4),
+                         "peak_source": tsrc, "kernel": "prefill_kernel<128, half>"},
+            "flops": fl, "us_with_append": round(us_append, 1),
+            "note": "fp16, 32 heads x D 128, causal, keys read through 16-token pages"}
+        if only == "prefill":
+            return res
+    # the small-page reproduction shapes: 4 x 170 new tokens over a cached prefix
+    w = wl.prefill_append(device=dev, seed=1004)
+    out = torch.empty_like(w["q"])
+    fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                   w["block_table"], k=w["k_new"], v=w["v_new"], causal=True,
+                                   out=out, return_lse=False)
+    us = time_calls(fn, 50, 5, stream)
+    old = w["cache_seqlens"].cpu().tolist()
+    fl = attention_flops([170] * 4, [o + 170 for o in old], 32, 128, True)
+    res["prefill_append_4x170"] = {"us": round(us, 1), "tflops": round(fl / us / 1e6, 2),
+                                   "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4)}
+    if only not in (None, "gqa"):
+        return res
+    # GQA split-KV decode on a contiguous 131072-token cache, lengths U[1024, 8192]
+    w = wl.gqa_contiguous(device=dev)
+    kc = torch.empty((8, w["capacity"], 8, 128), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    n = w["k_rows"].shape[1]
+    kc[:, :n] = w["k_rows"]
+    vc[:, :n] = w["v_rows"]
+    del w["k_rows"], w["v_rows"]
+    out = torch.empty_like(w["q"])
+    lse = torch.empty((8, 32, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, pa.fwd_kvcache_workspace_size(8, 1, 32, 8, 128, w["capacity"], 0)),
+                     dtype=torch.uint8, device=dev)
+    fn = lambda: pa.pa_fwd_kvcache(w["q"], kc, vc, w["cache_seqlens"], None, out=out, lse=lse,  # noqa: E731
+                                   workspace=ws)
+    us = time_calls(fn, 100 if only is None else 3, 10 if only is None else 3, stream,
+                    graph=only is None)
+    lens = w["cache_seqlens"].cpu().tolist()
+    by = sum(lens) * 8 * 128 * 2 * 2 + 8 * 32 * 128 * 2 * 2
+    res["gqa_contiguous_split_kv"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
+                                      "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4),
+                                      "mean_len": sum(lens) / len(lens)}
+    del kc, vc
+    if only == "gqa":
+        return res
+    # tiny paged decode (launch-latency bound)
+    w = wl.tiny_decode(device=dev)
+    fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                   w["block_table"], scale=w["scale"])
+    res["tiny_decode"] = {"us": round(time_calls(fn, 200, 20, stream), 2)}
+    return res
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for name in ("decode.cu", "pa_common.cuh", "pa_internal.h"):
@@ -267,6 +412,10 @@ def main():
     ap.add_argument("--batch", type=int, default=WORKLOAD["batch"],
                     help="smaller batches are for profiling runs only")
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the other configurations (prefill, GQA split-KV, tiny decode)")
+    ap.add_argument("--only", choices=["prefill", "gqa"],
+                    help="time only this secondary leg (for profiling runs)")
     args = ap.parse_args()
     WORKLOAD["batch"], WORKLOAD["ctx"] = args.batch, args.ctx
     args.warmup = max(3, args.warmup)
@@ -290,6 +439,9 @@ def main():
     pa.load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.only:
+        print(json.dumps(secondary_measurements(dev, only=args.only)), flush=True)
+        return
     B, ctx, lnew = WORKLOAD["batch"], WORKLOAD["ctx"], WORKLOAD["lnew"]
     hq, hkv, d = WORKLOAD["num_q_heads"], WORKLOAD["num_kv_heads"], WORKLOAD["head_dim"]
     # each rank is an independent replica with its own sequences (weak scaling)
@@ -387,6 +539,11 @@ def main():
         cpu = None
         if not args.no_cpu_baseline and world >= 1:
             cpu = cpu_baseline(w)
+        secondary = None
+        if not args.no_secondary:
+            del w
+            torch.cuda.empty_cache()
+            secondary = secondary_measurements(dev)
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
@@ -404,6 +561,7 @@ def main():
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "cpu_baseline": cpu,
+            "secondary": secondary,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

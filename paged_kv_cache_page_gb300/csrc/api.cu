@@ -11,7 +11,7 @@
 #include <string>
 
 #include "pa_internal.h"
-#include "pa_prefill.h"
+#include "pa_engine.h"
 
 namespace pa {
 namespace {
@@ -40,6 +40,9 @@ bool mult8(int64_t s) { return s > 0 && (s % 8) == 0; }
 constexpr int kSplitCapTargetCtas = 304;  // 152 SMs x 2 resident decode CTAs
 constexpr int kMinChunkPages = 8;         // each split streams >= 128 keys
 constexpr int kMaxSplits = 128;
+// Query blocks of at most this many rows per kv head run on the CUDA-core
+// split-KV decode kernel; larger ones on the tensor-core engine.
+constexpr int kCudaCoreRows = 2;
 
 int plan_s_max(int B, int Hkv, int max_seqlen_k, int num_splits) {
   const int max_pages = std::max(1, (max_seqlen_k + kPage - 1) / kPage);
@@ -142,24 +145,32 @@ int num_sms() {
   return sms[dev];
 }
 
-bool encode_cache_map(CUtensorMap* map, const void* base, int dtype, int D, int Hkv, int64_t dim2,
-                      int64_t dim3, int64_t stride_h, int64_t stride_t, int64_t stride_b,
-                      int box_d, int box_rows, bool swizzle128) {
+bool encode_map(CUtensorMap* map, const void* base, int dtype, int D, int H, int64_t dim2,
+                int64_t dim3, int64_t stride_h, int64_t stride_t, int64_t stride_b, int box_d,
+                int box_h, int box_rows, bool swz = true) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode_fn();
   if (fn == nullptr) return false;
-  (void)dtype;
-  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)dim2, (cuuint64_t)dim3};
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)dim2, (cuuint64_t)dim3};
   const cuuint64_t strides[3] = {(cuuint64_t)stride_h * 2, (cuuint64_t)stride_t * 2,
                                  (cuuint64_t)stride_b * 2};
-  const cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t box[4] = {(cuuint32_t)box_d, (cuuint32_t)box_h, (cuuint32_t)box_rows, 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  // swz: 128-byte swizzle (64-column boxes for the tensor cores); the
+  // CUDA-core decode reads unswizzled full-row boxes.
   const CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_cache_map(CUtensorMap* map, const void* base, int dtype, int D, int Hkv, int64_t dim2,
+                      int64_t dim3, int64_t stride_h, int64_t stride_t, int64_t stride_b,
+                      int box_d, int box_rows, bool swizzle128) {
+  return encode_map(map, base, dtype, D, Hkv, dim2, dim3, stride_h, stride_t, stride_b, box_d, 1,
+                    box_rows, swizzle128);
 }
 
 }  // namespace pa
@@ -211,8 +222,11 @@ PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_ne
 PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int D,
                                             int max_seqlen_k, int num_splits) {
   if (B <= 0 || Lq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
-  const int rows = Lq * (Hq / Hkv);
-  if (rows > kDecodeMaxRows) return 0;  // tensor-core path needs no workspace
+  const int G = Hq / Hkv;
+  const int rows = Lq * G;
+  // split partials exist for the CUDA-core decode and for packed engine items;
+  // 128-row tiles of one head are never split
+  if (rows > kEngineMaxRows || (rows > kCudaCoreRows && kEngineMaxRows % G != 0)) return 0;
   const int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
   return split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max).total;
 }
@@ -261,41 +275,75 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   const int G = Hq / Hkv;
   const int rows = Lq * G;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (rows > kDecodeMaxRows) {
-    // Tensor-core prefill: the new tokens are appended first (same stream),
-    // then every key is read from the cache.
+  if (rows > kCudaCoreRows) {
+    // Tensor-core engine: the new tokens are appended first (same stream),
+    // then every key is read from the cache.  Query blocks of up to 128 rows
+    // per kv head run packed (all G heads of a kv head in one tile, split-KV);
+    // longer ones as 128-row tiles of one head.
     if (Lnew > 0) {
       rc = pa_append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table, bt_stride,
                         max_pages, B, Lnew, Hkv, D, cache_extent, dtype, err_word, stream);
       if (rc) return rc;
     }
+    const bool pack = rows <= kEngineMaxRows && (kEngineMaxRows % G) == 0;
+    const int s_max = pack ? plan_s_max(B, Hkv, max_seqlen_k, num_splits) : 1;
+    const SplitWorkspace ws = split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max);
+    if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
+      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
+                  workspace_bytes);
     const bool paged_p = block_table != nullptr;
-    CUtensorMap tq, tk, tv;
-    if (!encode_cache_map(&tq, q, dtype, D, Hq, Lq, B, q_sh, q_st, q_sb, 64, 128, true) ||
-        !encode_cache_map(&tk, k_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
-                          paged_p ? cache_extent : B, k_cache.stride_h, k_cache.stride_t,
-                          k_cache.stride_b, 64, kPage, true) ||
-        !encode_cache_map(&tv, v_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
-                          paged_p ? cache_extent : B, v_cache.stride_h, v_cache.stride_t,
-                          v_cache.stride_b, 64, kPage, true))
+    CUtensorMap tq1, tq2, tk, tv;
+    if (!encode_map(&tq1, q, dtype, D, Hq, Lq, B, q_sh, q_st, q_sb, 64, 1, 128) ||
+        !encode_map(&tq2, q, dtype, D, Hq, Lq, B, q_sh, q_st, q_sb, 64, pack ? G : 1,
+                    pack ? kEngineMaxRows / G : 128) ||
+        !encode_map(&tk, k_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
+                    paged_p ? cache_extent : B, k_cache.stride_h, k_cache.stride_t,
+                    k_cache.stride_b, 64, 1, kPage) ||
+        !encode_map(&tv, v_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
+                    paged_p ? cache_extent : B, v_cache.stride_h, v_cache.stride_t,
+                    v_cache.stride_b, 64, 1, kPage))
       return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for q or the caches");
-    PrefillParams pp{};
-    pp.out = out;
-    pp.lse = lse;
-    pp.cache_seqlens = cache_seqlens;
-    pp.Lnew = Lnew;
-    pp.block_table = block_table;
-    pp.bt_stride = bt_stride;
-    pp.max_pages = paged_p ? max_pages : 0;
-    pp.extent = cache_extent;
-    pp.B = B; pp.Lq = Lq; pp.Hq = Hq; pp.Hkv = Hkv; pp.G = G;
-    pp.max_seqlen_k = max_seqlen_k;
-    pp.q_tiles = (Lq + 127) / 128;
-    pp.scale_log2 = scale * kLog2e;
-    pp.causal = causal ? 1 : 0;
-    pp.err = err_word;
-    const cudaError_t e = launch_prefill(pp, tq, tk, tv, D, dtype, st);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    const int grid = engine_grid();
+    EngineParams ep{};
+    ep.out = out;
+    ep.lse = lse;
+    ep.cache_seqlens = cache_seqlens;
+    ep.Lnew = Lnew;
+    ep.block_table = block_table;
+    ep.bt_stride = bt_stride;
+    ep.max_pages = paged_p ? max_pages : 0;
+    ep.extent = cache_extent;
+    ep.B = B; ep.Lq = Lq; ep.Hq = Hq; ep.Hkv = Hkv; ep.G = G;
+    ep.max_seqlen_k = max_seqlen_k;
+    ep.total_q = 0;
+    ep.pack_rows = pack ? kEngineMaxRows : 0;
+    ep.max_q_tiles = (Lq + kEngineMaxRows - 1) / kEngineMaxRows;
+    ep.scale_log2 = scale * kLog2e;
+    ep.causal = causal ? 1 : 0;
+    ep.s_max = s_max;
+    ep.target_ctas = num_splits > 0 ? (1 << 30) : 2 * grid;
+    ep.min_chunk_pages = num_splits > 0 ? 1 : kMinChunkPages;
+    uint8_t* wsb = reinterpret_cast<uint8_t*>(workspace);
+    ep.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
+    ep.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
+    ep.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
+    ep.err = err_word;
+    cudaError_t e = launch_engine(ep, tq1, tq2, tk, tv, D, dtype, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "engine launch");
+    if (s_max > 1) {
+      CombineParams c{};
+      c.o_part = ep.o_part;
+      c.lse_part = ep.lse_part;
+      c.nsplit = ep.nsplit;
+      c.S = s_max;
+      c.B = B; c.Lq = Lq; c.Hq = Hq;
+      c.cu_seqlens_q = nullptr;
+      c.total_q = 0;
+      c.out = out;
+      c.lse = lse;
+      e = launch_combine(c, D, dtype, B * Lq, st);
+      if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    }
     return PA_OK;
   }
 
@@ -392,60 +440,59 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
   if (max_pages < 1 || bt_stride < max_pages || num_pages < 1)
     return fail(PA_ERR_INVALID_ARG, "block table / pool sizes");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale");
-  if (B > kDecodeMaxSchedB) return fail(PA_ERR_UNSUPPORTED, "more than %d sequences", kDecodeMaxSchedB);
+  if (B > kEngineMaxB) return fail(PA_ERR_UNSUPPORTED, "more than %d sequences", kEngineMaxB);
   const int G = Hq / Hkv;
-  if (max_seqlen_q * G > kDecodeMaxRows)
-    return fail(PA_ERR_UNSUPPORTED, "prefill sequences in the unified launch");
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int rmax = kDecodeMaxRows;
-  const int s_max = plan_s_max(B, Hkv, max_seqlen_k, 0);
+  // One engine launch over the whole mixed batch: sequences of up to 128
+  // query rows per kv head (decode, multi-query decode, short chunks) run as
+  // packed split-KV items, longer chunks as 128-row tiles of one head.
+  const bool pack = (kEngineMaxRows % G) == 0;
+  const int s_max = pack ? plan_s_max(B, Hkv, max_seqlen_k, 0) : 1;
   const SplitWorkspace ws = split_workspace_layout(B, total_q, Hq, D, s_max);
   if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
                 workspace_bytes);
-  CUtensorMap tmk, tmv;
-  if (!encode_cache_map(&tmk, k_cache.ptr, dtype, D, Hkv, kPage, num_pages, k_cache.stride_h,
-                        k_cache.stride_t, k_cache.stride_b, D, kPage, false) ||
-      !encode_cache_map(&tmv, v_cache.ptr, dtype, D, Hkv, kPage, num_pages, v_cache.stride_h,
-                        v_cache.stride_t, v_cache.stride_b, D, kPage, false))
-    return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for the cache views");
-  DecodeParams p{};
-  p.q = q;
-  p.q_sb = 0; p.q_st = q_st; p.q_sh = q_sh;
-  p.out = out;
-  p.lse = lse;
-  p.k_cache = k_cache.ptr;
-  p.v_cache = v_cache.ptr;
-  p.k_sb = k_cache.stride_b; p.k_st = k_cache.stride_t; p.k_sh = k_cache.stride_h;
-  p.v_sb = v_cache.stride_b; p.v_st = v_cache.stride_t; p.v_sh = v_cache.stride_h;
-  p.block_table = block_table;
-  p.bt_stride = bt_stride;
-  p.max_pages = max_pages;
-  p.extent = num_pages;
-  p.cu_seqlens_q = cu_seqlens_q;
-  p.seqlens_k = seqlens_k;
-  p.B = B; p.Lq = 0; p.Hq = Hq; p.Hkv = Hkv; p.G = G;
-  p.max_seqlen_k = max_seqlen_k;
-  p.total_q = total_q;
-  p.scale_log2 = scale * kLog2e;
-  p.causal = causal ? 1 : 0;
-  p.s_max = s_max;
-  const int resident = decode_resident_ctas(D, dtype, rmax);
-  p.target_ctas = resident;
-  p.grid_ctas = resident;
-  p.min_chunk_pages = kMinChunkPages;
+  CUtensorMap tq1, tq2, tk, tv;
+  if (!encode_map(&tq1, q, dtype, D, Hq, total_q, 1, q_sh, q_st, q_st * total_q, 64, 1, 128) ||
+      !encode_map(&tq2, q, dtype, D, Hq, total_q, 1, q_sh, q_st, q_st * total_q, 64,
+                  pack ? G : 1, pack ? kEngineMaxRows / G : 128) ||
+      !encode_map(&tk, k_cache.ptr, dtype, D, Hkv, kPage, num_pages, k_cache.stride_h,
+                  k_cache.stride_t, k_cache.stride_b, 64, 1, kPage) ||
+      !encode_map(&tv, v_cache.ptr, dtype, D, Hkv, kPage, num_pages, v_cache.stride_h,
+                  v_cache.stride_t, v_cache.stride_b, 64, 1, kPage))
+    return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for q or the caches");
+  const int grid = engine_grid();
+  EngineParams ep{};
+  ep.out = out;
+  ep.lse = lse;
+  ep.cu_seqlens_q = cu_seqlens_q;
+  ep.seqlens_k = seqlens_k;
+  ep.block_table = block_table;
+  ep.bt_stride = bt_stride;
+  ep.max_pages = max_pages;
+  ep.extent = num_pages;
+  ep.B = B; ep.Lq = 0; ep.Hq = Hq; ep.Hkv = Hkv; ep.G = G;
+  ep.max_seqlen_k = max_seqlen_k;
+  ep.total_q = total_q;
+  ep.pack_rows = pack ? kEngineMaxRows : 0;
+  ep.max_q_tiles = (max_seqlen_q + kEngineMaxRows - 1) / kEngineMaxRows;
+  ep.scale_log2 = scale * kLog2e;
+  ep.causal = causal ? 1 : 0;
+  ep.s_max = s_max;
+  ep.target_ctas = 2 * grid;
+  ep.min_chunk_pages = kMinChunkPages;
   uint8_t* wsb = reinterpret_cast<uint8_t*>(workspace);
-  p.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
-  p.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
-  p.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
-  p.err = err_word;
-  cudaError_t e = launch_decode(p, tmk, tmv, D, dtype, rmax, st);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  ep.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
+  ep.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
+  ep.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
+  ep.err = err_word;
+  cudaError_t e = launch_engine(ep, tq1, tq2, tk, tv, D, dtype, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "engine launch");
   if (s_max > 1) {
     CombineParams c{};
-    c.o_part = p.o_part;
-    c.lse_part = p.lse_part;
-    c.nsplit = p.nsplit;
+    c.o_part = ep.o_part;
+    c.lse_part = ep.lse_part;
+    c.nsplit = ep.nsplit;
     c.S = s_max;
     c.B = B; c.Lq = 0; c.Hq = Hq;
     c.cu_seqlens_q = cu_seqlens_q;
@@ -457,6 +504,7 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
   }
   return PA_OK;
 }
+
 
 PA_API int pa_split_combine(const float* o_partial, const float* lse_partial,
                             const int32_t* splits_per_seq, int S, int B, int Lq, int Hq, int D,

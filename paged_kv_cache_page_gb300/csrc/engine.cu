@@ -1,0 +1,725 @@
+// Persistent tensor-core attention engine over a paged KV cache (sm_103a).
+//
+// One launch walks a work list that every CTA derives on the GPU from the
+// sequence lengths (no host read of lengths: flash-attention #1000
+// "Inappropriate Number of Splits ...").  Two kinds of items:
+//   kind 0  a 128-row query tile of ONE query head (long prefills): keys
+//           [0, causal limit of the tile) -- the flash_attn_with_kvcache
+//           prefill of flash-attention #824 "Add support for small page sizes".
+//   kind 1  the q_len * G query rows (<= 128) of ALL G query heads that share
+//           one kv head, packed into one tile (GQA packing: K/V streamed once
+//           per kv head), against one split of the keys; split outputs go to
+//           partials that the combine kernel merges -- decode, multi-query
+//           decode and short chunked prefills.
+// A varlen batch may mix both kinds in one launch: the unified launch of vLLM
+// #6052 "Unify the kernel used in flash attention backend".
+//
+// CTA = 192 threads, one per SM, persistent over items:
+//   warps 0-3  softmax: thread r owns tile row r (= TMEM lane r).  S from TMEM,
+//              masking, running max / sum in the log2 domain, P (fp16/bf16)
+//              to shared memory in the 128-byte-swizzled K-major layout, lazy
+//              O rescale (only when the max grows by more than 2^8), epilogue.
+//   warp 4     TMA producer: Q of the item, then per 128-key tile 8 pages of K
+//              and V, each page resolved absolutely from the block table.
+//   warp 5     TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
+//              buffers (tile j+1 issued before P V of tile j), O += P V.
+// TMEM: S0 cols [0,128), S1 [128,256), O [256, 256+D).  Pipeline state
+// (stage and buffer parities) runs on across items.
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_engine.h"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kBM = 128;                 // tile rows
+constexpr int kBN = 128;                 // keys per KV tile
+constexpr int kTilePages = kBN / kPage;  // 8
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct EngTraits {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kSlab = 128 * 128;  // one 128-row x 128-byte slab
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kQBytes = kHalves * kSlab;
+  static constexpr int kKVBytes = kHalves * kSlab;
+  static constexpr int kPBytes = 2 * kSlab;  // 128 keys
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;
+  static constexpr int kOffP = kOffV + kStages * kKVBytes;
+  static constexpr int kOffPre = kOffP + kPBytes;  // two int[kEngineMaxB + 1] prefix sums
+  static constexpr int kOffBar = kOffPre + ((2 * (kEngineMaxB + 1) * 4 + 15) & ~15);
+  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct SeqI {
+  int qlen, lk;
+  int64_t row0;  // global row index of query 0 (output / partial addressing)
+  int qcoord;    // TMA row coordinate of query 0
+  int qb;        // TMA batch coordinate
+};
+
+__device__ __forceinline__ SeqI seq_of(const EngineParams& p, int b, bool rep) {
+  SeqI s;
+  int old;
+  if (p.cu_seqlens_q != nullptr) {
+    const int q0 = __ldg(p.cu_seqlens_q + b);
+    s.qlen = __ldg(p.cu_seqlens_q + b + 1) - q0;
+    s.lk = __ldg(p.seqlens_k + b);
+    old = s.lk;
+    s.row0 = q0;
+    s.qcoord = q0;
+    s.qb = 0;
+  } else {
+    s.qlen = p.Lq;
+    old = __ldg(p.cache_seqlens + b);
+    s.lk = old + p.Lnew;
+    s.row0 = (int64_t)b * p.Lq;
+    s.qcoord = 0;
+    s.qb = b;
+  }
+  bool bad = old < 0 || s.lk < 0 || s.lk > p.max_seqlen_k || s.qlen < 0;
+  if (p.block_table != nullptr)
+    bad = bad || (int64_t)(s.lk + kPage - 1) / kPage > p.max_pages;
+  else
+    bad = bad || (int64_t)s.lk > p.extent;
+  if (bad) {
+    if (rep) report(p.err, PA_DEVERR_LENGTH, b, s.qlen < 0 ? s.qlen : s.lk);
+    s.lk = 0;
+    if (s.qlen < 0) s.qlen = 0;
+  }
+  return s;
+}
+
+__device__ __forceinline__ bool packed_seq(const EngineParams& p, int qlen) {
+  return qlen > 0 && qlen * p.G <= p.pack_rows;
+}
+
+// Pages per split of a packed sequence (a multiple of one 8-page KV tile) and
+// the split count.
+__device__ __forceinline__ int packed_split(const EngineParams& p, int pages, int chunk,
+                                            int* n_out) {
+  if (p.s_max <= 1 || pages <= 0) {
+    *n_out = 1;
+    return pages > 0 ? pages : 0;
+  }
+  int n = (pages + chunk - 1) / chunk;
+  n = max(1, min(n, p.s_max));
+  int per = (pages + n - 1) / n;
+  per = (per + kTilePages - 1) / kTilePages * kTilePages;
+  *n_out = (pages + per - 1) / per;
+  return per;
+}
+
+struct Item {
+  int kind, b, head, qs, nrows, qlen, lk, k0, k1, ntiles, split, nsplit;
+  int64_t row0;
+  int qcoord, qb;
+};
+
+struct Sched {
+  bool uniform;   // kvcache call: every sequence has the same query length
+  bool packed_u;  // uniform and packed
+  int total0, total1, chunk;
+  const int* pre0;
+  const int* pre1;
+};
+
+__device__ __forceinline__ int last_le(const int* pre, int n, int x) {
+  int lo = 0, hi = n;  // last index in [0, n) with pre[idx] <= x
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc, int idx) {
+  Item it;
+  int b, head, t = 0, s = 0;
+  bool packed;
+  if (sc.uniform) {
+    packed = sc.packed_u;
+    if (packed) {
+      const int per_b = p.Hkv * max(1, p.s_max);
+      b = idx / per_b;
+      const int li = idx % per_b;
+      s = li / p.Hkv;
+      head = li % p.Hkv;
+    } else {
+      const int qt = p.max_q_tiles;
+      const int bh = idx / qt;
+      t = qt - 1 - idx % qt;
+      b = bh / p.Hq;
+      head = bh % p.Hq;
+    }
+  } else if (idx < sc.total0) {
+    packed = false;
+    b = last_le(sc.pre0, p.B, idx);
+    const int li = idx - sc.pre0[b];
+    const SeqI q = seq_of(p, b, false);
+    const int qt = (q.qlen + kBM - 1) / kBM;
+    head = li / qt;
+    t = qt - 1 - li % qt;
+  } else {
+    packed = true;
+    const int i1 = idx - sc.total0;
+    b = last_le(sc.pre1, p.B, i1);
+    const int li = i1 - sc.pre1[b];
+    s = li / p.Hkv;
+    head = li % p.Hkv;
+  }
+  const SeqI q = seq_of(p, b, true);
+  it.b = b;
+  it.head = head;
+  it.qlen = q.qlen;
+  it.lk = q.lk;
+  it.row0 = q.row0;
+  it.qcoord = q.qcoord;
+  it.qb = q.qb;
+  if (!packed) {
+    it.kind = 0;
+    it.qs = t * kBM;
+    it.nrows = max(0, min(kBM, q.qlen - it.qs));
+    it.k0 = 0;
+    int k1 = q.lk;
+    if (p.causal) k1 = min(q.lk, it.qs + it.nrows + q.lk - q.qlen);
+    it.k1 = max(0, k1);
+    if (it.nrows == 0) it.k1 = 0;
+    it.split = 0;
+    it.nsplit = 1;
+  } else {
+    it.kind = 1;
+    it.qs = 0;
+    it.nrows = q.qlen * p.G;
+    const int pages = (q.lk + kPage - 1) / kPage;
+    int n;
+    const int per = packed_split(p, pages, sc.chunk, &n);
+    it.split = s;
+    it.nsplit = n;
+    it.k0 = min(s * per * kPage, q.lk);
+    it.k1 = min((s + 1) * per * kPage, q.lk);
+    if (s >= n) it.k1 = it.k0;  // uniform mode: splits past this sequence's count are empty
+  }
+  it.ntiles = it.k1 > it.k0 ? (it.k1 - it.k0 + kBN - 1) / kBN : 0;
+  return it;
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(192, 1)
+    engine_kernel(const EngineParams p, const __grid_constant__ CUtensorMap tm_q1,
+                  const __grid_constant__ CUtensorMap tm_q2,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v) {
+  using Tr = EngTraits<D>;
+  using E = Elem<T>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem + Tr::kOffQ;
+  uint8_t* sK = smem + Tr::kOffK;
+  uint8_t* sV = smem + Tr::kOffV;
+  uint8_t* sP = smem + Tr::kOffP;
+  int* pre0 = reinterpret_cast<int*>(smem + Tr::kOffPre);
+  int* pre1 = pre0 + (kEngineMaxB + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* v_full = k_full + Tr::kStages;
+  uint64_t* k_empty = v_full + Tr::kStages;
+  uint64_t* v_empty = k_empty + Tr::kStages;
+  uint64_t* s_full = v_empty + Tr::kStages;  // [2]
+  uint64_t* s_free = s_full + 2;             // [2]
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint64_t* o_free = pv_done + 1;
+  uint64_t* mma_fin = o_free + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Tr::kOffMisc);
+  int* misc = reinterpret_cast<int*>(smem + Tr::kOffMisc + 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < Tr::kStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(o_free, 4);
+    mbar_init(mma_fin, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(tslot, Tr::kTmemCols);
+    tc::tmem_relinquish();
+  }
+
+  // ---- device schedule
+  Sched sc;
+  sc.uniform = p.cu_seqlens_q == nullptr && (p.s_max <= 1 || !(p.Lq > 0 && p.Lq * p.G <= p.pack_rows));
+  sc.packed_u = p.cu_seqlens_q == nullptr && p.Lq > 0 && p.Lq * p.G <= p.pack_rows;
+  sc.pre0 = pre0;
+  sc.pre1 = pre1;
+  sc.chunk = 0;
+  if (sc.uniform) {
+    sc.total0 = sc.packed_u ? 0 : p.B * p.Hq * p.max_q_tiles;
+    sc.total1 = sc.packed_u ? p.B * p.Hkv * max(1, p.s_max) : 0;
+  } else {
+    long long part = 0;
+    for (int b = tid; b < p.B; b += 192) {
+      const SeqI q = seq_of(p, b, true);
+      if (packed_seq(p, q.qlen)) part += (q.lk + kPage - 1) / kPage;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    long long* red = reinterpret_cast<long long*>(sP);  // P is free before the first tile
+    if (lane == 0) red[warp] = part;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < 6; ++w) total += red[w];
+    {
+      long long slots = (long long)p.target_ctas;
+      long long c = (total * p.Hkv + slots - 1) / max(1LL, slots);
+      if (c < p.min_chunk_pages) c = p.min_chunk_pages;
+      if (c > (1 << 28)) c = 1 << 28;
+      sc.chunk = (int)((c + kTilePages - 1) / kTilePages * kTilePages);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int carry0 = 0, carry1 = 0;
+      for (int base = 0; base < p.B; base += 32) {
+        const int b = base + lane;
+        int c0 = 0, c1 = 0;
+        if (b < p.B) {
+          const SeqI q = seq_of(p, b, false);
+          if (packed_seq(p, q.qlen)) {
+            int n;
+            packed_split(p, (q.lk + kPage - 1) / kPage, sc.chunk, &n);
+            c1 = n * p.Hkv;
+          } else if (q.qlen > 0) {
+            c0 = (q.qlen + kBM - 1) / kBM * p.Hq;
+          }
+        }
+        int i0 = c0, i1 = c1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y0 = __shfl_up_sync(0xffffffffu, i0, o);
+          const int y1 = __shfl_up_sync(0xffffffffu, i1, o);
+          if (lane >= o) {
+            i0 += y0;
+            i1 += y1;
+          }
+        }
+        if (b < p.B) {
+          pre0[b] = carry0 + i0 - c0;
+          pre1[b] = carry1 + i1 - c1;
+        }
+        carry0 += __shfl_sync(0xffffffffu, i0, 31);
+        carry1 += __shfl_sync(0xffffffffu, i1, 31);
+      }
+      if (lane == 0) {
+        pre0[p.B] = carry0;
+        pre1[p.B] = carry1;
+        misc[0] = carry0;
+        misc[1] = carry1;
+      }
+    }
+    __syncthreads();
+    sc.total0 = misc[0];
+    sc.total1 = misc[1];
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS[2] = {tbase, tbase + 128};
+  const uint32_t tO = tbase + 256;
+  const int total = sc.total0 + sc.total1;
+
+  if (warp == 4) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, 0, 0};
+      bool failed = false;
+      int tctr = 0, a = 0;
+      for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
+        const Item it = get_item(p, sc, idx);
+        if (it.ntiles == 0) continue;
+        if (a >= 1 && !failed && !mbar_wait(q_empty, (uint32_t)((a - 1) & 1))) {
+          report(p.err, PA_DEVERR_TIMEOUT, it.b, -1);
+          failed = true;
+        }
+        mbar_arrive_expect_tx(q_full, Tr::kQBytes);
+        for (int hh = 0; hh < Tr::kHalves; ++hh) {
+          if (it.kind == 0)
+            tma_load_4d(sQ + hh * Tr::kSlab, &tm_q1, q_full, hh * 64, it.head,
+                        it.qcoord + it.qs, it.qb, pol_q);
+          else
+            tma_load_4d(sQ + hh * Tr::kSlab, &tm_q2, q_full, hh * 64, it.head * p.G, it.qcoord,
+                        it.qb, pol_q);
+        }
+        const int g = it.kind == 0 ? it.head / p.G : it.head;
+        const int pg_begin = it.k0 / kPage;
+        const int pg_end = (it.k1 + kPage - 1) / kPage;
+        for (int j = 0; j < it.ntiles; ++j) {
+          const int Tj = tctr + j;
+          const int s = Tj % Tr::kStages;
+          const uint32_t par = (uint32_t)((Tj / Tr::kStages) & 1);
+          const int pg0 = pg_begin + j * kTilePages;
+          const int npg = min(kTilePages, pg_end - pg0);
+          int c2[kTilePages], c3[kTilePages];
+          for (int i = 0; i < npg; ++i) {
+            const PageRef r = resolve_page(geom, it.b, pg0 + i);
+            if (!r.ok) report(p.err, PA_DEVERR_PAGE_OOB, it.b, pg0 + i);
+            c2[i] = r.c2;
+            c3[i] = r.c3;
+          }
+          if (!failed && !mbar_wait(&k_empty[s], par ^ 1)) {
+            report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
+            failed = true;
+          }
+          mbar_arrive_expect_tx(&k_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
+          for (int i = 0; i < npg; ++i)
+            for (int hh = 0; hh < Tr::kHalves; ++hh)
+              tma_load_4d(sK + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_k, &k_full[s],
+                          hh * 64, g, c2[i], c3[i], pol_kv);
+          if (!failed && !mbar_wait(&v_empty[s], par ^ 1)) {
+            report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
+            failed = true;
+          }
+          mbar_arrive_expect_tx(&v_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
+          for (int i = 0; i < npg; ++i)
+            for (int hh = 0; hh < Tr::kHalves; ++hh)
+              tma_load_4d(sV + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_v, &v_full[s],
+                          hh * 64, g, c2[i], c3[i], pol_kv);
+        }
+        tctr += it.ntiles;
+        ++a;
+      }
+    }
+  } else if (warp == 5) {
+    // ======================= MMA issuer =======================
+    bool failed = false;
+    auto wait = [&](uint64_t* bar, uint32_t par, int where) {
+      if (!failed && !mbar_wait(bar, par)) {
+        report(p.err, PA_DEVERR_TIMEOUT, -1, where);
+        failed = true;
+      }
+    };
+    const bool bf = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t id_qk = tc::idesc_f16(kBM, kBN, bf, false);
+    const uint32_t id_pv = tc::idesc_f16(kBM, D, bf, true);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+    int tctr = 0, a = 0;
+    for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
+      const Item it = get_item(p, sc, idx);
+      if (it.ntiles == 0) continue;
+      auto issue_qk = [&](int jq) {
+        const int Tq = tctr + jq;
+        const int s = Tq % Tr::kStages;
+        wait(&k_full[s], (uint32_t)((Tq / Tr::kStages) & 1), 100);
+        if (Tq >= 2) wait(&s_free[Tq & 1], (uint32_t)(((Tq - 2) >> 1) & 1), 200);
+        tc::fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Tr::kSlab + (kk & 3) * 32;
+            tc::mma_f16_ss(tS[Tq & 1], tc::smem_desc(aQ + off, 16, 1024),
+                           tc::smem_desc(aK + s * Tr::kKVBytes + off, 16, 1024), id_qk, kk > 0);
+          }
+          tc::commit(&s_full[Tq & 1]);
+          tc::commit(&k_empty[s]);
+          if (jq == it.ntiles - 1) tc::commit(q_empty);  // Q no longer read
+        }
+        __syncwarp();
+      };
+      wait(q_full, (uint32_t)(a & 1), 50);
+      issue_qk(0);
+      for (int j = 0; j < it.ntiles; ++j) {
+        const int Tj = tctr + j;
+        if (j + 1 < it.ntiles) issue_qk(j + 1);
+        const int s = Tj % Tr::kStages;
+        wait(p_full, (uint32_t)(Tj & 1), 300);
+        wait(&v_full[s], (uint32_t)((Tj / Tr::kStages) & 1), 400);
+        if (j == 0 && a >= 1) wait(o_free, (uint32_t)((a - 1) & 1), 450);
+        // keys past the item's range: zero their V rows so P = 0 never meets a
+        // stale or non-finite value
+        const int valid = it.k1 - (it.k0 + j * kBN);
+        if (valid < kBN) {
+          uint8_t* vt = sV + s * Tr::kKVBytes;
+          const int nrow = kBN - valid;
+          for (int e = lane; e < nrow * Tr::kHalves * 8; e += 32) {
+            const int r = valid + e / (Tr::kHalves * 8);
+            const int rest = e % (Tr::kHalves * 8);
+            *reinterpret_cast<uint4*>(vt + (rest >> 3) * Tr::kSlab + r * 128 + (rest & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc::fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint32_t offp = (kk >> 2) * Tr::kSlab + (kk & 3) * 32;
+            tc::mma_f16_ss(tO, tc::smem_desc(aP + offp, 16, 1024),
+                           tc::smem_desc(aV + s * Tr::kKVBytes + kk * 2048, Tr::kSlab, 1024),
+                           id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(pv_done);
+          tc::commit(&v_empty[s]);
+        }
+        __syncwarp();
+      }
+      tctr += it.ntiles;
+      ++a;
+    }
+    // every tcgen05 operation of this thread has completed once this arrives
+    if (lane == 0) tc::commit(mma_fin);
+    __syncwarp();
+    wait(mma_fin, 0, 900);
+  } else {
+    // ======================= softmax warps 0-3 =======================
+    const int r = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float sc_l2 = p.scale_log2;
+    bool failed = false;
+    auto wait = [&](uint64_t* bar, uint32_t par, int where) {
+      if (!failed && !mbar_wait(bar, par)) {
+        report(p.err, PA_DEVERR_TIMEOUT, -1, where);
+        failed = true;
+      }
+    };
+    int tctr = 0, a = 0;
+    for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
+      const Item it = get_item(p, sc, idx);
+      // row geometry
+      const bool valid = r < it.nrows;
+      int qi, h;
+      if (it.kind == 0) {
+        qi = it.qs + r;
+        h = it.head;
+      } else {
+        qi = r / p.G;
+        h = it.head * p.G + r % p.G;
+      }
+      int vis_end = p.causal ? min(it.k1, qi + it.lk - it.qlen + 1) : it.k1;
+      if (!valid) vis_end = it.k0;
+      const bool to_partial = it.kind == 1 && it.nsplit > 1;
+      if (it.kind == 1 && it.split == 0 && it.head == 0 && r == 0 && p.nsplit != nullptr)
+        p.nsplit[it.b] = to_partial ? it.nsplit : 0;
+      const int64_t grow = it.row0 + qi;  // global output row
+      auto write_row = [&](const float* ov, int c, float inv) {
+        if (to_partial) {
+          float* dst = p.o_part +
+                       (((int64_t)it.split * (p.cu_seqlens_q ? p.total_q : (int64_t)p.B * p.Lq) +
+                         grow) * p.Hq + h) * D + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + i) =
+                make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
+        } else {
+          T* dst = reinterpret_cast<T*>(p.out) + (grow * p.Hq + h) * D + c * 32;
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 u;
+            u.x = E::from_f2(ov[i] * inv, ov[i + 1] * inv);
+            u.y = E::from_f2(ov[i + 2] * inv, ov[i + 3] * inv);
+            u.z = E::from_f2(ov[i + 4] * inv, ov[i + 5] * inv);
+            u.w = E::from_f2(ov[i + 6] * inv, ov[i + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + i) = u;
+          }
+        }
+      };
+      auto write_lse = [&](float v) {
+        if (to_partial) {
+          p.lse_part[((int64_t)it.split * (p.cu_seqlens_q ? p.total_q : (int64_t)p.B * p.Lq) +
+                      grow) * p.Hq + h] = v;
+        } else if (p.lse != nullptr) {
+          if (p.cu_seqlens_q)
+            p.lse[(int64_t)h * p.total_q + grow] = v;
+          else
+            p.lse[((int64_t)it.b * p.Hq + h) * p.Lq + qi] = v;
+        }
+      };
+      if (it.ntiles == 0) {
+        if (valid) {
+          float z[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = 0.f;
+          for (int c = 0; c < D / 32; ++c) write_row(z, c, 0.f);
+          write_lse(neg_inf());
+        }
+        continue;
+      }
+      float m_use = neg_inf(), l = 0.f;
+      for (int j = 0; j < it.ntiles; ++j) {
+        const int Tj = tctr + j;
+        const uint32_t tSj = tS[Tj & 1] + lane_off;
+        wait(&s_full[Tj & 1], (uint32_t)((Tj >> 1) & 1), 500);
+        tc::fence_after_sync();
+        const int lim = vis_end - (it.k0 + j * kBN);  // keys [0, lim) of this tile are visible
+        const bool full_tile = lim >= kBN;
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = neg_inf();
+#pragma unroll 1
+        for (int c = 0; c < kBN / 64; ++c) {
+          float v[64];
+          tc::tmem_ld32(tSj + c * 64, v);
+          tc::tmem_ld32(tSj + c * 64 + 32, v + 32);
+          tc::tmem_wait_ld();
+          if (full_tile) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              mx8[i & 7] = (c * 64 + i < lim) ? fmaxf(mx8[i & 7], v[i]) : mx8[i & 7];
+          }
+        }
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        if (mx != neg_inf()) mx *= sc_l2;
+        const float m_new = fmaxf(m_use, mx);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_new != neg_inf() && (m_use == neg_inf() || m_new > m_use + kRescaleThreshold)) {
+          if (m_use != neg_inf()) {
+            alpha = ex2(m_use - m_new);
+            rescale = true;
+          }
+          l *= alpha;
+          m_use = m_new;
+        }
+        // P buffer and O are free / stable once PV of the previous tile is done
+        if (Tj >= 1) wait(pv_done, (uint32_t)((Tj - 1) & 1), 600);
+        uint8_t* prow = sP + r * 128;
+        const float neg_m = -m_use;
+        float rs8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 64; ++c) {
+          float v[64];
+          tc::tmem_ld32(tSj + c * 64, v);
+          tc::tmem_ld32(tSj + c * 64 + 32, v + 32);
+          tc::tmem_wait_ld();
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float e0 = ex2(fmaf(v[2 * i], sc_l2, neg_m));
+            float e1 = ex2(fmaf(v[2 * i + 1], sc_l2, neg_m));
+            if (!full_tile) {
+              e0 = (c * 64 + 2 * i < lim) ? e0 : 0.f;
+              e1 = (c * 64 + 2 * i + 1 < lim) ? e1 : 0.f;
+            }
+            rs8[i & 7] += e0 + e1;
+            pk[i] = E::from_f2(e0, e1);
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(prow + c * Tr::kSlab + ((c8 ^ (r & 7)) << 4)) =
+                make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+        }
+        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[Tj & 1]);
+        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+          const float sa = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float ov[32];
+            tc::tmem_ld32(tO + lane_off + c * 32, ov);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] *= sa;
+            tc::tmem_st32(tO + lane_off + c * 32, ov);
+          }
+          tc::tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      // ---- epilogue
+      wait(pv_done, (uint32_t)((tctr + it.ntiles - 1) & 1), 700);
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        tc::tmem_ld32(tO + lane_off + c * 32, ov);
+        tc::tmem_wait_ld();
+        if (valid) write_row(ov, c, inv);
+      }
+      if (valid) write_lse(l > 0.f ? (m_use + lg2(l)) * kLn2 : neg_inf());
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      tctr += it.ntiles;
+      ++a;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 5) tc::tmem_dealloc(tbase, Tr::kTmemCols);
+}
+
+template <int D, typename T>
+cudaError_t launch_t(const EngineParams& p, const CUtensorMap& q1, const CUtensorMap& q2,
+                     const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
+  using Tr = EngTraits<D>;
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        engine_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  engine_kernel<D, T><<<grid, 192, Tr::kSmemBytes, st>>>(p, q1, q2, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int engine_grid() { return num_sms(); }
+
+cudaError_t launch_engine(const EngineParams& p, const CUtensorMap& tm_q1,
+                          const CUtensorMap& tm_q2, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, int D, int dtype, int grid, cudaStream_t st) {
+  if (grid < 1) grid = 1;
+  if (D == 128 && dtype == PA_F16) return launch_t<128, __half>(p, tm_q1, tm_q2, tm_k, tm_v, grid, st);
+  if (D == 128 && dtype == PA_BF16)
+    return launch_t<128, __nv_bfloat16>(p, tm_q1, tm_q2, tm_k, tm_v, grid, st);
+  if (D == 64 && dtype == PA_F16) return launch_t<64, __half>(p, tm_q1, tm_q2, tm_k, tm_v, grid, st);
+  if (D == 64 && dtype == PA_BF16)
+    return launch_t<64, __nv_bfloat16>(p, tm_q1, tm_q2, tm_k, tm_v, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

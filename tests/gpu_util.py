@@ -65,3 +65,26 @@ def assert_close(out, lse, ref_out, ref_lse, dtype, rows=None):
             lerr = np.abs(l[fin] - ref_lse[fin]).max()
             assert lerr <= LSE_TOL, f"max |LSE - oracle| = {lerr:.3e}"
     return err
+
+
+def oracle_varlen(w, seqs=None):
+    """Oracle for a varlen workload dict, one sequence at a time (only the
+    pages each sequence uses are copied to the host).  Returns
+    {b: (O [qlen, Hq, D], LSE [Hq, qlen])}."""
+    cu = w["cu_seqlens_q"].cpu().tolist()
+    lens = w["seqlens_k"].cpu().tolist()
+    table = w["block_table"]
+    res = {}
+    for b in (range(len(lens)) if seqs is None else seqs):
+        q0, q1 = cu[b], cu[b + 1]
+        if q1 == q0:
+            continue
+        npg = -(-lens[b] // 16)
+        pages = table[b, :npg].long()
+        kc = np64(w["k_cache"][pages])
+        vc = np64(w["v_cache"][pages])
+        o, l = oracle.fwd_varlen(np64(w["q"][q0:q1]), kc, vc, [0, q1 - q0], [lens[b]],
+                                 np.arange(max(npg, 1))[None], scale=w["scale"],
+                                 causal=w["causal"])
+        res[b] = (o, l)
+    return res

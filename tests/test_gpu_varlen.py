@@ -1,0 +1,74 @@
+"""GPU parity of the unified varlen launch (pa_fwd_varlen_unified): one
+launch over chunked-prefill and decode sequences of a paged cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_page_gb300 as pa
+from paged_kv_cache_page_gb300 import workloads as wl
+
+from gpu_util import LSE_TOL, OUT_TOL, np64, oracle_varlen
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run(w):
+    err = pa.new_err_word(DEV)
+    out = torch.full_like(w["q"], float("nan"))
+    lse = torch.full((w["q"].shape[1], w["q"].shape[0]), float("nan"), device=DEV)
+    pa.pa_fwd_varlen_unified(w["q"], w["k_cache"], w["v_cache"], w["cu_seqlens_q"],
+                             w["seqlens_k"], w["block_table"], w["max_seqlen_q"],
+                             w["max_seqlen_k"], scale=w["scale"], causal=w["causal"], out=out,
+                             lse=lse, err=err)
+    torch.cuda.synchronize()
+    assert err[0].item() == 0, err.tolist()
+    return out, lse
+
+
+def check(w, out, lse, dtype, seqs=None):
+    ref = oracle_varlen(w, seqs)
+    cu = w["cu_seqlens_q"].cpu().tolist()
+    worst = 0.0
+    for b, (ro, rl) in ref.items():
+        o = np64(out[cu[b]:cu[b + 1]])
+        l = np64(lse[:, cu[b]:cu[b + 1]])
+        e = np.abs(o - ro).max()
+        worst = max(worst, e)
+        assert e <= OUT_TOL[dtype], (b, e)
+        fin = np.isfinite(rl)
+        assert np.array_equal(np.isfinite(l), fin)
+        if fin.any():
+            assert np.abs(l[fin] - rl[fin]).max() <= LSE_TOL, b
+    return worst
+
+
+@pytest.mark.parametrize("heads,d", [(12, 64), (32, 128), (64, 128)])
+def test_unified_mixed_batch(heads, d):
+    """Chunked prefills of 100 / 500 / 1000 query tokens over cached prefixes
+    U[0, 2048] plus 64 decodes with contexts U[1024, 4096], causal, bf16."""
+    w = wl.unified_mixed(num_heads=heads, head_dim=d, device=DEV, seed=1005 + heads)
+    out, lse = run(w)
+    # every prefill sequence and a sample of the decodes
+    check(w, out, lse, "bf16", seqs=[0, 1, 2, 3, 17, 40, 66])
+
+
+def test_unified_gqa_and_padding_entries():
+    w = wl.unified_mixed(num_heads=16, num_kv_heads=4, head_dim=128, prefill_lens=(7, 40, 300),
+                         prefix_hi=700, num_decode=9, ctx_lo=1, ctx_hi=900, pad_to=16,
+                         device=DEV, seed=77)
+    out, lse = run(w)
+    check(w, out, lse, "bf16")
+    # padding sequences own no rows: every row of the batch was written
+    assert torch.isfinite(out).all()
+
+
+def test_unified_zero_length_keys_and_single_key():
+    w = wl.unified_mixed(num_heads=4, head_dim=64, prefill_lens=(5,), prefix_hi=0,
+                         num_decode=3, ctx_lo=1, ctx_hi=1, device=DEV, seed=78)
+    w["seqlens_k"][1] = 0  # a decode sequence with no keys at all
+    out, lse = run(w)
+    cu = w["cu_seqlens_q"].cpu().tolist()
+    assert torch.all(out[cu[1]] == 0) and torch.all(torch.isneginf(lse[:, cu[1]]))
+    check(w, out, lse, "bf16", seqs=[0, 2, 3])
