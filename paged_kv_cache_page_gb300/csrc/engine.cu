@@ -14,14 +14,15 @@
 // A varlen batch may mix both kinds in one launch: the unified launch of vLLM
 // #6052 "Unify the kernel used in flash attention backend".
 //
-// CTA = 192 threads, one per SM, persistent over items:
-//   warps 0-3  softmax: thread r owns tile row r (= TMEM lane r).  S from TMEM,
+// CTA = 320 threads, one per SM, persistent over items:
+//   warps 0-7  softmax: warps w and w+4 share tile rows 32(w%4).. (their TMEM
+//              lane quarter), each taking 64 of the 128 columns.  S from TMEM,
 //              masking, running max / sum in the log2 domain, P (fp16/bf16)
 //              to shared memory in the 128-byte-swizzled K-major layout, lazy
 //              O rescale (only when the max grows by more than 2^8), epilogue.
-//   warp 4     TMA producer: Q of the item, then per 128-key tile 8 pages of K
+//   warp 8     TMA producer: Q of the item, then per 128-key tile 8 pages of K
 //              and V, each page resolved absolutely from the block table.
-//   warp 5     TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
+//   warp 9     TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
 //              buffers (tile j+1 issued before P V of tile j), O += P V.
 // TMEM: S0 cols [0,128), S1 [128,256), O [256, 256+D).  Pipeline state
 // (stage and buffer parities) runs on across items.
@@ -39,6 +40,10 @@ constexpr int kBM = 128;                 // tile rows
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kTilePages = kBN / kPage;  // 8
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
+constexpr int kWarpTMA = kSoftWarps;        // TMA producer warp
+constexpr int kWarpMMA = kSoftWarps + 1;    // MMA issuer + TMEM owner
+constexpr int kThreads = (kSoftWarps + 2) * 32;
 
 template <int D>
 struct EngTraits {
@@ -55,7 +60,8 @@ struct EngTraits {
   static constexpr int kOffPre = kOffP + kPBytes;  // two int[kEngineMaxB + 1] prefix sums
   static constexpr int kOffBar = kOffPre + ((2 * (kEngineMaxB + 1) * 4 + 15) & ~15);
   static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 1 + 1 + 1 + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffX = (kOffBar + kNumBars * 8 + 15) & ~15;  // row max / sum exchange
+  static constexpr int kOffMisc = kOffX + (2 * 2 * 128 + 128) * 4;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
 };
@@ -214,7 +220,7 @@ __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc,
 }
 
 template <int D, typename T>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     engine_kernel(const EngineParams p, const __grid_constant__ CUtensorMap tm_q1,
                   const __grid_constant__ CUtensorMap tm_q2,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -259,15 +265,15 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+      mbar_init(&s_free[i], kSoftWarps);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, kSoftWarps);
     mbar_init(pv_done, 1);
-    mbar_init(o_free, 4);
+    mbar_init(o_free, kSoftWarps);
     mbar_init(mma_fin, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMMA) {
     tc::tmem_alloc(tslot, Tr::kTmemCols);
     tc::tmem_relinquish();
   }
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(192, 1)
     sc.total1 = sc.packed_u ? p.B * p.Hkv * max(1, p.s_max) : 0;
   } else {
     long long part = 0;
-    for (int b = tid; b < p.B; b += 192) {
+    for (int b = tid; b < p.B; b += kThreads) {
       const SeqI q = seq_of(p, b, true);
       if (packed_seq(p, q.qlen)) part += (q.lk + kPage - 1) / kPage;
     }
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) red[warp] = part;
     __syncthreads();
     long long total = 0;
-    for (int w = 0; w < 6; ++w) total += red[w];
+    for (int w = 0; w < kThreads / 32; ++w) total += red[w];
     {
       long long slots = (long long)p.target_ctas;
       long long c = (total * p.Hkv + slots - 1) / max(1LL, slots);
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tO = tbase + 256;
   const int total = sc.total0 + sc.total1;
 
-  if (warp == 4) {
+  if (warp == kWarpTMA) {
     // ======================= TMA producer =======================
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(192, 1)
         ++a;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMMA) {
     // ======================= MMA issuer =======================
     bool failed = false;
     auto wait = [&](uint64_t* bar, uint32_t par, int where) {
@@ -499,10 +505,18 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
     wait(mma_fin, 0, 900);
   } else {
-    // ======================= softmax warps 0-3 =======================
-    const int r = tid;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ======================= softmax warps 0-7 =======================
+    // Warps w and w+4 own tile rows 32*(w%4) .. +31 (the TMEM lane quarter a
+    // warp may access); warp w < 4 takes S columns 0-63 and O columns
+    // [0, D/2), warp w >= 4 columns 64-127 and [D/2, D).  The two halves of a
+    // row agree on the running max through shared memory and keep separate
+    // partial sums, added at the end.
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int r = quarter * 32 + lane;  // tile row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sc_l2 = p.scale_log2;
+    float* xmax = reinterpret_cast<float*>(smem + Tr::kOffX);  // [2 parity][2 half][128]
+    float* xl = xmax + 2 * 2 * 128;                             // [128]
     bool failed = false;
     auto wait = [&](uint64_t* bar, uint32_t par, int where) {
       if (!failed && !mbar_wait(bar, par)) {
@@ -510,11 +524,13 @@ __global__ void __launch_bounds__(192, 1)
         failed = true;
       }
     };
+    auto pair_sync = [&]() { named_barrier(1 + quarter, 64); };
+    constexpr int kDH = D / 2;  // O columns per half
     int tctr = 0, a = 0;
     for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
       const Item it = get_item(p, sc, idx);
-      // row geometry
       const bool valid = r < it.nrows;
+      const bool quarter_live = quarter * 32 < it.nrows;  // any valid row in this quarter
       int qi, h;
       if (it.kind == 0) {
         qi = it.qs + r;
@@ -526,20 +542,20 @@ __global__ void __launch_bounds__(192, 1)
       int vis_end = p.causal ? min(it.k1, qi + it.lk - it.qlen + 1) : it.k1;
       if (!valid) vis_end = it.k0;
       const bool to_partial = it.kind == 1 && it.nsplit > 1;
-      if (it.kind == 1 && it.split == 0 && it.head == 0 && r == 0 && p.nsplit != nullptr)
+      if (it.kind == 1 && it.split == 0 && it.head == 0 && tid == 0 && p.nsplit != nullptr)
         p.nsplit[it.b] = to_partial ? it.nsplit : 0;
-      const int64_t grow = it.row0 + qi;  // global output row
-      auto write_row = [&](const float* ov, int c, float inv) {
+      const int64_t grow = it.row0 + qi;
+      const int64_t nrows_all = p.cu_seqlens_q ? (int64_t)p.total_q : (int64_t)p.B * p.Lq;
+      auto write_half = [&](const float* ov, int c, float inv) {  // 32 columns at hf*kDH + c*32
+        const int col = hf * kDH + c * 32;
         if (to_partial) {
-          float* dst = p.o_part +
-                       (((int64_t)it.split * (p.cu_seqlens_q ? p.total_q : (int64_t)p.B * p.Lq) +
-                         grow) * p.Hq + h) * D + c * 32;
+          float* dst = p.o_part + (((int64_t)it.split * nrows_all + grow) * p.Hq + h) * D + col;
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
             *reinterpret_cast<float4*>(dst + i) =
                 make_float4(ov[i] * inv, ov[i + 1] * inv, ov[i + 2] * inv, ov[i + 3] * inv);
         } else {
-          T* dst = reinterpret_cast<T*>(p.out) + (grow * p.Hq + h) * D + c * 32;
+          T* dst = reinterpret_cast<T*>(p.out) + (grow * p.Hq + h) * D + col;
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 u;
@@ -553,8 +569,7 @@ __global__ void __launch_bounds__(192, 1)
       };
       auto write_lse = [&](float v) {
         if (to_partial) {
-          p.lse_part[((int64_t)it.split * (p.cu_seqlens_q ? p.total_q : (int64_t)p.B * p.Lq) +
-                      grow) * p.Hq + h] = v;
+          p.lse_part[((int64_t)it.split * nrows_all + grow) * p.Hq + h] = v;
         } else if (p.lse != nullptr) {
           if (p.cu_seqlens_q)
             p.lse[(int64_t)h * p.total_q + grow] = v;
@@ -567,40 +582,45 @@ __global__ void __launch_bounds__(192, 1)
           float z[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) z[i] = 0.f;
-          for (int c = 0; c < D / 32; ++c) write_row(z, c, 0.f);
-          write_lse(neg_inf());
+          for (int c = 0; c < kDH / 32; ++c) write_half(z, c, 0.f);
+          if (hf == 0) write_lse(neg_inf());
         }
         continue;
       }
       float m_use = neg_inf(), l = 0.f;
       for (int j = 0; j < it.ntiles; ++j) {
         const int Tj = tctr + j;
-        const uint32_t tSj = tS[Tj & 1] + lane_off;
+        const uint32_t tSj = tS[Tj & 1] + lane_off + hf * 64;
         wait(&s_full[Tj & 1], (uint32_t)((Tj >> 1) & 1), 500);
         tc::fence_after_sync();
-        const int lim = vis_end - (it.k0 + j * kBN);  // keys [0, lim) of this tile are visible
-        const bool full_tile = lim >= kBN;
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = neg_inf();
-#pragma unroll 1
-        for (int c = 0; c < kBN / 64; ++c) {
-          float v[64];
-          tc::tmem_ld32(tSj + c * 64, v);
-          tc::tmem_ld32(tSj + c * 64 + 32, v + 32);
+        // keys [0, lim) of this half's 64 columns are visible to the row
+        const int lim = vis_end - (it.k0 + j * kBN + hf * 64);
+        const bool full = lim >= 64;
+        float v[64];
+        float mx = neg_inf();
+        if (quarter_live) {
+          tc::tmem_ld32(tSj, v);
+          tc::tmem_ld32(tSj + 32, v + 32);
           tc::tmem_wait_ld();
-          if (full_tile) {
+          float mx8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = neg_inf();
+          if (full) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], v[i]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-              mx8[i & 7] = (c * 64 + i < lim) ? fmaxf(mx8[i & 7], v[i]) : mx8[i & 7];
+            for (int i = 0; i < 64; ++i) mx8[i & 7] = (i < lim) ? fmaxf(mx8[i & 7], v[i]) : mx8[i & 7];
           }
+          mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          if (mx != neg_inf()) mx *= sc_l2;
+          xmax[((Tj & 1) * 2 + hf) * 128 + r] = mx;
         }
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        if (mx != neg_inf()) mx *= sc_l2;
+        tc::fence_before_sync();
+        pair_sync();
+        if (quarter_live) mx = fmaxf(mx, xmax[((Tj & 1) * 2 + (hf ^ 1)) * 128 + r]);
+        // both halves of a row see the same maximum and decide alike
         const float m_new = fmaxf(m_use, mx);
         float alpha = 1.f;
         bool rescale = false;
@@ -614,48 +634,43 @@ __global__ void __launch_bounds__(192, 1)
         }
         // P buffer and O are free / stable once PV of the previous tile is done
         if (Tj >= 1) wait(pv_done, (uint32_t)((Tj - 1) & 1), 600);
-        uint8_t* prow = sP + r * 128;
-        const float neg_m = -m_use;
-        float rs8[8];
+        if (quarter_live) {
+          uint8_t* prow = sP + hf * Tr::kSlab + r * 128;
+          const float neg_m = -m_use;
+          float rs8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 64; ++c) {
-          float v[64];
-          tc::tmem_ld32(tSj + c * 64, v);
-          tc::tmem_ld32(tSj + c * 64 + 32, v + 32);
-          tc::tmem_wait_ld();
+          for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             float e0 = ex2(fmaf(v[2 * i], sc_l2, neg_m));
             float e1 = ex2(fmaf(v[2 * i + 1], sc_l2, neg_m));
-            if (!full_tile) {
-              e0 = (c * 64 + 2 * i < lim) ? e0 : 0.f;
-              e1 = (c * 64 + 2 * i + 1 < lim) ? e1 : 0.f;
+            if (!full) {
+              e0 = (2 * i < lim) ? e0 : 0.f;
+              e1 = (2 * i + 1 < lim) ? e1 : 0.f;
             }
             rs8[i & 7] += e0 + e1;
             pk[i] = E::from_f2(e0, e1);
           }
 #pragma unroll
           for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<uint4*>(prow + c * Tr::kSlab + ((c8 ^ (r & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
                 make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+          l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         }
-        l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_free[Tj & 1]);
-        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+        if (j >= 1 && quarter_live && __any_sync(0xffffffffu, rescale)) {
           const float sa = rescale ? alpha : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < kDH / 32; ++c) {
             float ov[32];
-            tc::tmem_ld32(tO + lane_off + c * 32, ov);
+            const uint32_t ta = tO + lane_off + hf * kDH + c * 32;
+            tc::tmem_ld32(ta, ov);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] *= sa;
-            tc::tmem_st32(tO + lane_off + c * 32, ov);
+            tc::tmem_st32(ta, ov);
           }
           tc::tmem_wait_st();
         }
@@ -664,18 +679,25 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
       }
-      // ---- epilogue
+      // ---- epilogue: the two halves' sums, then O / l and LSE
+      if (hf == 1) xl[r] = l;
+      pair_sync();
+      if (hf == 0) xl[r] = l + xl[r];
+      pair_sync();
+      const float L = xl[r];
       wait(pv_done, (uint32_t)((tctr + it.ntiles - 1) & 1), 700);
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      if (quarter_live) {
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tc::tmem_ld32(tO + lane_off + c * 32, ov);
-        tc::tmem_wait_ld();
-        if (valid) write_row(ov, c, inv);
+        for (int c = 0; c < kDH / 32; ++c) {
+          float ov[32];
+          tc::tmem_ld32(tO + lane_off + hf * kDH + c * 32, ov);
+          tc::tmem_wait_ld();
+          if (valid) write_half(ov, c, inv);
+        }
+        if (valid && hf == 0) write_lse(L > 0.f ? (m_use + lg2(L)) * kLn2 : neg_inf());
       }
-      if (valid) write_lse(l > 0.f ? (m_use + lg2(l)) * kLn2 : neg_inf());
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free);
@@ -687,7 +709,7 @@ __global__ void __launch_bounds__(192, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 5) tc::tmem_dealloc(tbase, Tr::kTmemCols);
+  if (warp == kWarpMMA) tc::tmem_dealloc(tbase, Tr::kTmemCols);
 }
 
 template <int D, typename T>
@@ -701,7 +723,7 @@ cudaError_t launch_t(const EngineParams& p, const CUtensorMap& q1, const CUtenso
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  engine_kernel<D, T><<<grid, 192, Tr::kSmemBytes, st>>>(p, q1, q2, tk, tv);
+  engine_kernel<D, T><<<grid, kThreads, Tr::kSmemBytes, st>>>(p, q1, q2, tk, tv);
   return cudaGetLastError();
 }
 
