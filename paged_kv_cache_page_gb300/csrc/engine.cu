@@ -148,10 +148,20 @@ __device__ __forceinline__ int last_le(const int* pre, int n, int x) {
   return lo;
 }
 
-__device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc, int idx) {
+// Work unit `idx`, sub-item u (0 or 1).  A kind-0 unit is a PAIR of query
+// tiles of one head, t and q_tiles-1-t (heaviest with lightest under causal
+// masking), so every unit costs about the same: CTAs walking units
+// round-robin stay in step, and the query tiles of a head stream its K/V
+// through L2 together.  Kind-1 units have one item; their second sub-item (and
+// the second of an odd middle pair) is empty (kind -1, no rows, no tiles).
+__device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc, int idx, int u) {
   Item it;
   int b, head, t = 0, s = 0;
-  bool packed;
+  bool packed, null_item = false;
+  auto pick_pair = [&](int qt, int pi) {
+    t = (u == 0) ? qt - 1 - pi : pi;
+    null_item = (u == 1 && pi == qt - 1 - pi);
+  };
   if (sc.uniform) {
     packed = sc.packed_u;
     if (packed) {
@@ -160,10 +170,12 @@ __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc,
       const int li = idx % per_b;
       s = li / p.Hkv;
       head = li % p.Hkv;
+      null_item = u == 1;
     } else {
       const int qt = p.max_q_tiles;
-      const int bh = idx / qt;
-      t = qt - 1 - idx % qt;
+      const int pp = (qt + 1) / 2;
+      const int bh = idx / pp;
+      pick_pair(qt, idx % pp);
       b = bh / p.Hq;
       head = bh % p.Hq;
     }
@@ -173,8 +185,9 @@ __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc,
     const int li = idx - sc.pre0[b];
     const SeqI q = seq_of(p, b, false);
     const int qt = (q.qlen + kBM - 1) / kBM;
-    head = li / qt;
-    t = qt - 1 - li % qt;
+    const int pp = (qt + 1) / 2;
+    head = li / pp;
+    pick_pair(qt, li % pp);
   } else {
     packed = true;
     const int i1 = idx - sc.total0;
@@ -182,6 +195,7 @@ __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc,
     const int li = i1 - sc.pre1[b];
     s = li / p.Hkv;
     head = li % p.Hkv;
+    null_item = u == 1;
   }
   const SeqI q = seq_of(p, b, true);
   it.b = b;
@@ -191,7 +205,14 @@ __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc,
   it.row0 = q.row0;
   it.qcoord = q.qcoord;
   it.qb = q.qb;
-  if (!packed) {
+  if (null_item) {
+    it.kind = -1;
+    it.qs = 0;
+    it.nrows = 0;
+    it.k0 = it.k1 = 0;
+    it.split = 0;
+    it.nsplit = 1;
+  } else if (!packed) {
     it.kind = 0;
     it.qs = t * kBM;
     it.nrows = max(0, min(kBM, q.qlen - it.qs));
@@ -286,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sc.pre1 = pre1;
   sc.chunk = 0;
   if (sc.uniform) {
-    sc.total0 = sc.packed_u ? 0 : p.B * p.Hq * p.max_q_tiles;
+    sc.total0 = sc.packed_u ? 0 : p.B * p.Hq * ((p.max_q_tiles + 1) / 2);
     sc.total1 = sc.packed_u ? p.B * p.Hkv * max(1, p.s_max) : 0;
   } else {
     long long part = 0;
@@ -321,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             packed_split(p, (q.lk + kPage - 1) / kPage, sc.chunk, &n);
             c1 = n * p.Hkv;
           } else if (q.qlen > 0) {
-            c0 = (q.qlen + kBM - 1) / kBM * p.Hq;
+            c0 = ((q.qlen + kBM - 1) / kBM + 1) / 2 * p.Hq;
           }
         }
         int i0 = c0, i1 = c1;
@@ -362,15 +383,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ======================= TMA producer =======================
-    if (lane == 0) {
-      const uint64_t pol_kv = l2_policy_evict_last();
-      const uint64_t pol_q = l2_policy_evict_first();
-      CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, 0, 0};
-      bool failed = false;
-      int tctr = 0, a = 0;
-      for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
-        const Item it = get_item(p, sc, idx);
-        if (it.ntiles == 0) continue;
+    // The whole warp runs the loop.  Block-table entries are loaded 32 pages
+    // (4 KV tiles) at a time, one lane per page, a batch ahead of use and with
+    // no dependent instruction until the tile is issued, so the table reads
+    // never sit on the copy path; every entry is validated when used.  Lane 0
+    // waits for free stages and issues the copies.
+    const uint64_t pol_kv = l2_policy_evict_last();
+    const uint64_t pol_q = l2_policy_evict_first();
+    const bool paged = p.block_table != nullptr;
+    bool failed = false;
+    int tctr = 0, a = 0;
+    for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+      const Item it = get_item(p, sc, wu >> 1, wu & 1);
+      if (it.ntiles == 0) continue;
+      const int g = it.kind == 0 ? it.head / p.G : it.head;
+      const int pg_begin = it.k0 / kPage;
+      const int pg_end = (it.k1 + kPage - 1) / kPage;
+      const int32_t* trow = paged ? p.block_table + (int64_t)it.b * p.bt_stride : nullptr;
+      auto load_batch = [&](int batch) -> int {  // raw entry of page pg_begin + 32*batch + lane
+        const int lp = pg_begin + 32 * batch + lane;
+        return (paged && lp < pg_end && lp < p.max_pages) ? __ldg(trow + lp) : 0;
+      };
+      int cur = load_batch(0);
+      int nxt = (it.ntiles > 4) ? load_batch(1) : 0;
+      if (lane == 0) {
         if (a >= 1 && !failed && !mbar_wait(q_empty, (uint32_t)((a - 1) & 1))) {
           report(p.err, PA_DEVERR_TIMEOUT, it.b, -1);
           failed = true;
@@ -384,44 +420,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sQ + hh * Tr::kSlab, &tm_q2, q_full, hh * 64, it.head * p.G, it.qcoord,
                         it.qb, pol_q);
         }
-        const int g = it.kind == 0 ? it.head / p.G : it.head;
-        const int pg_begin = it.k0 / kPage;
-        const int pg_end = (it.k1 + kPage - 1) / kPage;
-        for (int j = 0; j < it.ntiles; ++j) {
-          const int Tj = tctr + j;
-          const int s = Tj % Tr::kStages;
-          const uint32_t par = (uint32_t)((Tj / Tr::kStages) & 1);
-          const int pg0 = pg_begin + j * kTilePages;
-          const int npg = min(kTilePages, pg_end - pg0);
-          int c2[kTilePages], c3[kTilePages];
-          for (int i = 0; i < npg; ++i) {
-            const PageRef r = resolve_page(geom, it.b, pg0 + i);
-            if (!r.ok) report(p.err, PA_DEVERR_PAGE_OOB, it.b, pg0 + i);
-            c2[i] = r.c2;
-            c3[i] = r.c3;
+      }
+      __syncwarp();
+      for (int j = 0; j < it.ntiles; ++j) {
+        if (j > 0 && (j & 3) == 0) {
+          cur = nxt;
+          nxt = (j + 4 < it.ntiles) ? load_batch((j >> 2) + 1) : 0;
+        }
+        const int Tj = tctr + j;
+        const int s = Tj % Tr::kStages;
+        const uint32_t par = (uint32_t)((Tj / Tr::kStages) & 1);
+        const int pg0 = pg_begin + j * kTilePages;
+        const int npg = min(kTilePages, pg_end - pg0);
+        int c2[kTilePages], c3[kTilePages];
+#pragma unroll
+        for (int i = 0; i < kTilePages; ++i) {
+          const int raw = __shfl_sync(0xffffffffu, cur, (j & 3) * kTilePages + i);
+          const int lp = pg0 + i;
+          bool ok;
+          if (paged) {
+            ok = lp < p.max_pages && raw >= 0 && (int64_t)raw < p.extent;
+            c2[i] = 0;
+            c3[i] = ok ? raw : 0;
+          } else {
+            ok = (int64_t)lp * kPage < p.extent;
+            c2[i] = ok ? lp * kPage : 0;
+            c3[i] = it.b;
           }
+          if (i < npg && !ok && lane == 0) report(p.err, PA_DEVERR_PAGE_OOB, it.b, lp);
+        }
+        if (lane == 0) {
           if (!failed && !mbar_wait(&k_empty[s], par ^ 1)) {
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
           mbar_arrive_expect_tx(&k_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
-          for (int i = 0; i < npg; ++i)
-            for (int hh = 0; hh < Tr::kHalves; ++hh)
-              tma_load_4d(sK + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_k, &k_full[s],
-                          hh * 64, g, c2[i], c3[i], pol_kv);
+#pragma unroll
+          for (int i = 0; i < kTilePages; ++i)
+            if (i < npg)
+              for (int hh = 0; hh < Tr::kHalves; ++hh)
+                tma_load_4d(sK + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_k, &k_full[s],
+                            hh * 64, g, c2[i], c3[i], pol_kv);
           if (!failed && !mbar_wait(&v_empty[s], par ^ 1)) {
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
           mbar_arrive_expect_tx(&v_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
-          for (int i = 0; i < npg; ++i)
-            for (int hh = 0; hh < Tr::kHalves; ++hh)
-              tma_load_4d(sV + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_v, &v_full[s],
-                          hh * 64, g, c2[i], c3[i], pol_kv);
+#pragma unroll
+          for (int i = 0; i < kTilePages; ++i)
+            if (i < npg)
+              for (int hh = 0; hh < Tr::kHalves; ++hh)
+                tma_load_4d(sV + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_v, &v_full[s],
+                            hh * 64, g, c2[i], c3[i], pol_kv);
         }
-        tctr += it.ntiles;
-        ++a;
+        __syncwarp();
       }
+      tctr += it.ntiles;
+      ++a;
     }
   } else if (warp == kWarpMMA) {
     // ======================= MMA issuer =======================
@@ -437,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id_pv = tc::idesc_f16(kBM, D, bf, true);
     const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
     int tctr = 0, a = 0;
-    for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
-      const Item it = get_item(p, sc, idx);
+    for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+      const Item it = get_item(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
       auto issue_qk = [&](int jq) {
         const int Tq = tctr + jq;
@@ -527,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pair_sync = [&]() { named_barrier(1 + quarter, 64); };
     constexpr int kDH = D / 2;  // O columns per half
     int tctr = 0, a = 0;
-    for (int idx = blockIdx.x; idx < total; idx += gridDim.x) {
-      const Item it = get_item(p, sc, idx);
+    for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+      const Item it = get_item(p, sc, wu >> 1, wu & 1);
       const bool valid = r < it.nrows;
       const bool quarter_live = quarter * 32 < it.nrows;  // any valid row in this quarter
       int qi, h;
