@@ -449,30 +449,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (i < npg && !ok && lane == 0) report(p.err, PA_DEVERR_PAGE_OOB, it.b, lp);
         }
+        // one warp instruction issues all boxes of a tile: lane l copies page
+        // l % 8, 64-column slab l / 8
+        const int my_page = lane & (kTilePages - 1);
+        const int my_slab = lane / kTilePages;
+        const bool issuer = my_page < npg && my_slab < Tr::kHalves;
+        int mc2 = 0, mc3 = 0;
+#pragma unroll
+        for (int i = 0; i < kTilePages; ++i)
+          if (i == my_page) {
+            mc2 = c2[i];
+            mc3 = c3[i];
+          }
         if (lane == 0) {
           if (!failed && !mbar_wait(&k_empty[s], par ^ 1)) {
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
           mbar_arrive_expect_tx(&k_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
-#pragma unroll
-          for (int i = 0; i < kTilePages; ++i)
-            if (i < npg)
-              for (int hh = 0; hh < Tr::kHalves; ++hh)
-                tma_load_4d(sK + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_k, &k_full[s],
-                            hh * 64, g, c2[i], c3[i], pol_kv);
+        }
+        __syncwarp();
+        if (issuer)
+          tma_load_4d(sK + s * Tr::kKVBytes + my_slab * Tr::kSlab + my_page * 2048, &tm_k,
+                      &k_full[s], my_slab * 64, g, mc2, mc3, pol_kv);
+        __syncwarp();
+        if (lane == 0) {
           if (!failed && !mbar_wait(&v_empty[s], par ^ 1)) {
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
           mbar_arrive_expect_tx(&v_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
-#pragma unroll
-          for (int i = 0; i < kTilePages; ++i)
-            if (i < npg)
-              for (int hh = 0; hh < Tr::kHalves; ++hh)
-                tma_load_4d(sV + s * Tr::kKVBytes + hh * Tr::kSlab + i * 2048, &tm_v, &v_full[s],
-                            hh * 64, g, c2[i], c3[i], pol_kv);
         }
+        __syncwarp();
+        if (issuer)
+          tma_load_4d(sV + s * Tr::kKVBytes + my_slab * Tr::kSlab + my_page * 2048, &tm_v,
+                      &v_full[s], my_slab * 64, g, mc2, mc3, pol_kv);
         __syncwarp();
       }
       tctr += it.ntiles;
