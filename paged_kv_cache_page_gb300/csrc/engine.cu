@@ -41,9 +41,10 @@ constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kTilePages = kBN / kPage;  // 8
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
-constexpr int kWarpTMA = kSoftWarps;        // TMA producer warp
-constexpr int kWarpMMA = kSoftWarps + 1;    // MMA issuer + TMEM owner
-constexpr int kThreads = (kSoftWarps + 2) * 32;
+constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
+constexpr int kWarpTMA = kSoftWarps;        // first TMA producer warp
+constexpr int kWarpMMA = kSoftWarps + kProdWarps;  // MMA issuer + TMEM owner
+constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;
 
 template <int D>
 struct EngTraits {
@@ -279,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < Tr::kStages; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&v_full[i], 1);
+      mbar_init(&k_full[i], kProdWarps);
+      mbar_init(&v_full[i], kProdWarps);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
     }
@@ -381,9 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tO = tbase + 256;
   const int total = sc.total0 + sc.total1;
 
-  if (warp == kWarpTMA) {
-    // ======================= TMA producer =======================
-    // The whole warp runs the loop.  Block-table entries are loaded 32 pages
+  if (warp >= kWarpTMA && warp < kWarpMMA) {
+    // ======================= TMA producers =======================
+    // kProdWarps warps run the same loop and split every tile's page boxes
+    // round-robin (TMA issue throughput grows with the number of issuing
+    // warps); each arrives on the stage barrier with its share of the bytes.
+    // Within a warp:  Block-table entries are loaded 32 pages
     // (4 KV tiles) at a time, one lane per page, a batch ahead of use and with
     // no dependent instruction until the tile is issued, so the table reads
     // never sit on the copy path; every entry is validated when used.  Lane 0
@@ -391,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_kv = l2_policy_evict_last();
     const uint64_t pol_q = l2_policy_evict_first();
     const bool paged = p.block_table != nullptr;
+    const int pw = warp - kWarpTMA;
     bool failed = false;
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int cur = load_batch(0);
       int nxt = (it.ntiles > 4) ? load_batch(1) : 0;
-      if (lane == 0) {
+      if (pw == 0 && lane == 0) {
         if (a >= 1 && !failed && !mbar_wait(q_empty, (uint32_t)((a - 1) & 1))) {
           report(p.err, PA_DEVERR_TIMEOUT, it.b, -1);
           failed = true;
@@ -447,13 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             c2[i] = ok ? lp * kPage : 0;
             c3[i] = it.b;
           }
-          if (i < npg && !ok && lane == 0) report(p.err, PA_DEVERR_PAGE_OOB, it.b, lp);
+          if (i < npg && !ok && lane == 0 && pw == 0) report(p.err, PA_DEVERR_PAGE_OOB, it.b, lp);
         }
-        // one warp instruction issues all boxes of a tile: lane l copies page
-        // l % 8, 64-column slab l / 8
-        const int my_page = lane & (kTilePages - 1);
-        const int my_slab = lane / kTilePages;
-        const bool issuer = my_page < npg && my_slab < Tr::kHalves;
+        // box b = page (b % 8), 64-column slab (b / 8); this warp issues the
+        // boxes b = pw + kProdWarps * lane
+        const int my_box = pw + kProdWarps * lane;
+        const int my_page = my_box & (kTilePages - 1);
+        const int my_slab = my_box / kTilePages;
+        const bool issuer = my_slab < Tr::kHalves && my_page < npg;
+        const int my_count = __popc(__ballot_sync(0xffffffffu, issuer));
         int mc2 = 0, mc3 = 0;
 #pragma unroll
         for (int i = 0; i < kTilePages; ++i)
@@ -466,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
-          mbar_arrive_expect_tx(&k_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
+          mbar_arrive_expect_tx(&k_full[s], (uint32_t)(my_count * 2048));
         }
         __syncwarp();
         if (issuer)
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
-          mbar_arrive_expect_tx(&v_full[s], (uint32_t)(npg * Tr::kHalves * 2048));
+          mbar_arrive_expect_tx(&v_full[s], (uint32_t)(my_count * 2048));
         }
         __syncwarp();
         if (issuer)
