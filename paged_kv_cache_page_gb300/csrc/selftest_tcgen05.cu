@@ -3,6 +3,8 @@
 // library).  One CTA computes, for a 128-row A:
 //   C1 = A * B1^T   (A and B1 K-major, 128-byte swizzle; B1 loaded by TMA)
 //   C2 = A * B2     (B2 [K=128, N=D] stored N-contiguous: MN-major operand)
+//   C3 = A * B2     with A read from TMEM (written there by threads, two
+//                   16-bit elements per column) -- the P tile's layout
 // with A written to shared memory by threads in the swizzled K-major layout
 // (the path the prefill kernel's P tile takes) and B1/B2 fetched by TMA boxes
 // of 64 columns (the path of its K and V tiles).  Accumulators live in TMEM
@@ -21,6 +23,7 @@ using namespace pa;
 template <typename T, int D>
 __global__ void __launch_bounds__(192, 1)
     selftest_kernel(const T* __restrict__ A, float* __restrict__ C1, float* __restrict__ C2,
+                    float* __restrict__ C3,
                     const __grid_constant__ CUtensorMap tm_b1,
                     const __grid_constant__ CUtensorMap tm_b2, int32_t* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -59,6 +62,21 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = *tslot;
+  // A rows -> TMEM columns [384, 448): thread r (warps 0-3) owns lane r
+  if (tid < 128) {
+    const T* arow = A + tid * 128;
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16) + 384;
+    for (int c = 0; c < 2; ++c) {
+      uint32_t w[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(arow + c * 64 + 2 * i);
+      tc::tmem_st32u(lane_addr + c * 32, w);
+    }
+    tc::tmem_wait_st();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
   if (warp == 4 && lane == 0) {
     mbar_arrive_expect_tx(b_full, 32768 + (D / 64) * 16384);
@@ -94,6 +112,10 @@ __global__ void __launch_bounds__(192, 1)
       tc::mma_f16_ss(tbase + 128, tc::smem_desc(aA + offA, 16, 1024),
                      tc::smem_desc(aB2 + kk * 2048, 16384, 1024), id2, kk > 0);
     }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      tc::mma_f16_ts(tbase + 256, tbase + 384 + kk * 8,
+                     tc::smem_desc(aB2 + kk * 2048, 16384, 1024), id2, kk > 0);
     tc::commit(mma_done);
   }
   if (warp < 4) {
@@ -115,6 +137,13 @@ __global__ void __launch_bounds__(192, 1)
       tc::tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i) C2[row * D + c * 32 + i] = v[i];
+    }
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      tc::tmem_ld32(lane_addr + 256 + c * 32, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) C3[row * D + c * 32 + i] = v[i];
     }
   }
   tc::fence_before_sync();
@@ -142,8 +171,8 @@ bool encode2d(CUtensorMap* m, const void* base, int dtype, uint64_t cols, uint64
 }
 
 template <typename T, int D>
-int run(const void* A, const void* B1, const void* B2, float* C1, float* C2, int32_t* status,
-        cudaStream_t st) {
+int run(const void* A, const void* B1, const void* B2, float* C1, float* C2, float* C3,
+        int32_t* status, cudaStream_t st) {
   CUtensorMap m1, m2;
   if (!encode2d(&m1, B1, std::is_same<T, __nv_bfloat16>::value ? PA_BF16 : PA_F16, 128, 128) ||
       !encode2d(&m2, B2, std::is_same<T, __nv_bfloat16>::value ? PA_BF16 : PA_F16, D, 128))
@@ -152,19 +181,21 @@ int run(const void* A, const void* B1, const void* B2, float* C1, float* C2, int
   if (cudaFuncSetAttribute(selftest_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return -2;
-  selftest_kernel<T, D><<<1, 192, smem, st>>>(reinterpret_cast<const T*>(A), C1, C2, m1, m2,
-                                              status);
+  selftest_kernel<T, D><<<1, 192, smem, st>>>(reinterpret_cast<const T*>(A), C1, C2, C3, m1,
+                                              m2, status);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
 }  // namespace
 
 extern "C" __attribute__((visibility("default"))) int pa_selftest_tcgen05_gemm(
-    const void* A, const void* B1, const void* B2, float* C1, float* C2, int D, int dtype,
-    int32_t* status, cudaStream_t st) {
-  if (D == 128 && dtype == PA_F16) return run<__half, 128>(A, B1, B2, C1, C2, status, st);
-  if (D == 128 && dtype == PA_BF16) return run<__nv_bfloat16, 128>(A, B1, B2, C1, C2, status, st);
-  if (D == 64 && dtype == PA_F16) return run<__half, 64>(A, B1, B2, C1, C2, status, st);
-  if (D == 64 && dtype == PA_BF16) return run<__nv_bfloat16, 64>(A, B1, B2, C1, C2, status, st);
+    const void* A, const void* B1, const void* B2, float* C1, float* C2, float* C3, int D,
+    int dtype, int32_t* status, cudaStream_t st) {
+  if (D == 128 && dtype == PA_F16) return run<__half, 128>(A, B1, B2, C1, C2, C3, status, st);
+  if (D == 128 && dtype == PA_BF16)
+    return run<__nv_bfloat16, 128>(A, B1, B2, C1, C2, C3, status, st);
+  if (D == 64 && dtype == PA_F16) return run<__half, 64>(A, B1, B2, C1, C2, C3, status, st);
+  if (D == 64 && dtype == PA_BF16)
+    return run<__nv_bfloat16, 64>(A, B1, B2, C1, C2, C3, status, st);
   return -4;
 }

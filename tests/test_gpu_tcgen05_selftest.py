@@ -1,8 +1,9 @@
 """Encoding self-test of the tcgen05 operand layouts the prefill kernel uses
 (one CTA, one 128x128 tile) against a plain PyTorch fp32 matmul:
 C1 = A B1^T with both operands K-major and 128-byte swizzled (A written by
-threads like the P tile, B1 fetched by TMA like a K tile), and C2 = A B2 with
-B2 an MN-major operand (like a V tile)."""
+threads like the P tile, B1 fetched by TMA like a K tile), C2 = A B2 with
+B2 an MN-major operand (like a V tile), and C3 = A B2 with A read from tensor
+memory (like the P tile)."""
 
 import ctypes
 
@@ -27,9 +28,10 @@ def test_tcgen05_operand_layouts(dtype, d):
     B2 = torch.randn((128, d), generator=g, device=DEV).to(dtype)
     C1 = torch.full((128, 128), float("nan"), device=DEV)
     C2 = torch.full((128, d), float("nan"), device=DEV)
+    C3 = torch.full((128, d), float("nan"), device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
-    rc = lib.pa_selftest_tcgen05_gemm(p(A), p(B1), p(B2), p(C1), p(C2), d,
+    rc = lib.pa_selftest_tcgen05_gemm(p(A), p(B1), p(B2), p(C1), p(C2), p(C3), d,
                                       pa.PA_BF16 if dtype == torch.bfloat16 else pa.PA_F16,
                                       p(status), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
@@ -38,3 +40,4 @@ def test_tcgen05_operand_layouts(dtype, d):
     ref2 = A.float() @ B2.float()
     torch.testing.assert_close(C1, ref1, rtol=1e-4, atol=1e-3)
     torch.testing.assert_close(C2, ref2, rtol=1e-4, atol=1e-3)
+    torch.testing.assert_close(C3, ref2, rtol=1e-4, atol=1e-3)
