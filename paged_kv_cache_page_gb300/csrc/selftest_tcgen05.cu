@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(192, 1)
     selftest_kernel(const T* __restrict__ A, float* __restrict__ C1, float* __restrict__ C2,
                     float* __restrict__ C3,
                     const __grid_constant__ CUtensorMap tm_b1,
-                    const __grid_constant__ CUtensorMap tm_b2, int32_t* status) {
+                    const __grid_constant__ CUtensorMap tm_b2, int32_t* status, int a_col) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(arow + c * 64 + 2 * i);
       tc::tmem_st32u(lane_addr + c * 32, w);
+      tc::tmem_st32u(lane_addr + 64 + c * 32, w);  // second copy at column 448
     }
     tc::tmem_wait_st();
   }
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(192, 1)
     }
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      tc::mma_f16_ts(tbase + 256, tbase + 384 + kk * 8,
+      tc::mma_f16_ts(tbase + 256, tbase + a_col + kk * 8,
                      tc::smem_desc(aB2 + kk * 2048, 16384, 1024), id2, kk > 0);
     tc::commit(mma_done);
   }
@@ -172,7 +173,7 @@ bool encode2d(CUtensorMap* m, const void* base, int dtype, uint64_t cols, uint64
 
 template <typename T, int D>
 int run(const void* A, const void* B1, const void* B2, float* C1, float* C2, float* C3,
-        int32_t* status, cudaStream_t st) {
+        int32_t* status, int a_col, cudaStream_t st) {
   CUtensorMap m1, m2;
   if (!encode2d(&m1, B1, std::is_same<T, __nv_bfloat16>::value ? PA_BF16 : PA_F16, 128, 128) ||
       !encode2d(&m2, B2, std::is_same<T, __nv_bfloat16>::value ? PA_BF16 : PA_F16, D, 128))
@@ -182,7 +183,7 @@ int run(const void* A, const void* B1, const void* B2, float* C1, float* C2, flo
                            smem) != cudaSuccess)
     return -2;
   selftest_kernel<T, D><<<1, 192, smem, st>>>(reinterpret_cast<const T*>(A), C1, C2, C3, m1,
-                                              m2, status);
+                                              m2, status, a_col);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
@@ -190,12 +191,13 @@ int run(const void* A, const void* B1, const void* B2, float* C1, float* C2, flo
 
 extern "C" __attribute__((visibility("default"))) int pa_selftest_tcgen05_gemm(
     const void* A, const void* B1, const void* B2, float* C1, float* C2, float* C3, int D,
-    int dtype, int32_t* status, cudaStream_t st) {
-  if (D == 128 && dtype == PA_F16) return run<__half, 128>(A, B1, B2, C1, C2, C3, status, st);
+    int dtype, int32_t* status, int a_col, cudaStream_t st) {
+  if (a_col != 384 && a_col != 448) return -5;
+  if (D == 128 && dtype == PA_F16) return run<__half, 128>(A, B1, B2, C1, C2, C3, status, a_col, st);
   if (D == 128 && dtype == PA_BF16)
-    return run<__nv_bfloat16, 128>(A, B1, B2, C1, C2, C3, status, st);
-  if (D == 64 && dtype == PA_F16) return run<__half, 64>(A, B1, B2, C1, C2, C3, status, st);
+    return run<__nv_bfloat16, 128>(A, B1, B2, C1, C2, C3, status, a_col, st);
+  if (D == 64 && dtype == PA_F16) return run<__half, 64>(A, B1, B2, C1, C2, C3, status, a_col, st);
   if (D == 64 && dtype == PA_BF16)
-    return run<__nv_bfloat16, 64>(A, B1, B2, C1, C2, C3, status, st);
+    return run<__nv_bfloat16, 64>(A, B1, B2, C1, C2, C3, status, a_col, st);
   return -4;
 }

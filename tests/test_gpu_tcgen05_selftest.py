@@ -17,9 +17,10 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+@pytest.mark.parametrize("a_col", [384, 448])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("d", [64, 128])
-def test_tcgen05_operand_layouts(dtype, d):
+def test_tcgen05_operand_layouts(dtype, d, a_col):
     pabuild.build()
     lib = ctypes.CDLL(pabuild.lib_path(pabuild.SELFTEST_LIB))
     g = torch.Generator(device=DEV).manual_seed(d)
@@ -33,7 +34,8 @@ def test_tcgen05_operand_layouts(dtype, d):
     p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     rc = lib.pa_selftest_tcgen05_gemm(p(A), p(B1), p(B2), p(C1), p(C2), p(C3), d,
                                       pa.PA_BF16 if dtype == torch.bfloat16 else pa.PA_F16,
-                                      p(status), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                                      p(status), a_col,
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     assert rc == 0 and status.item() == 0
     ref1 = A.float() @ B1.float().T
