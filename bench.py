@@ -121,6 +121,65 @@ def time_calls(fn, steps, warmup, stream, graph=True):
     return e0.elapsed_time(e1) / steps * 1e3
 
 
+def decode_sweep(dev):
+    """The paged decode sweep: ctx {512..4096} x batch {1..256}, 32 q = 32 kv
+    heads, D 128, fp16, one appended token per sequence, automatic splits.
+    One JSON line per point with us per call, algorithmic GB/s and the
+    fraction of the HBM copy peak; points whose ideal time is under 20 us are
+    launch-latency bound and marked `graded: false`."""
+    import torch
+
+    import paged_kv_cache_page_gb300 as pa
+    from paged_kv_cache_page_gb300 import workloads as wl
+
+    peak, src = read_peaks()
+    stream = torch.cuda.current_stream(dev)
+    for ctx in (512, 1024, 2048, 4096):
+        for B in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+            w = wl.paged_decode(B, ctx, lnew=1, seed=1002, device=dev)
+            out = torch.empty((B, 1, 32, 128), dtype=torch.float16, device=dev)
+            lse = torch.empty((B, 32, 1), dtype=torch.float32, device=dev)
+            ws = torch.empty(max(1, pa.fwd_kvcache_workspace_size(B, 1, 32, 32, 128, ctx, 0)),
+                             dtype=torch.uint8, device=dev)
+            fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"],  # noqa: E731
+                                           w["cache_seqlens"], w["block_table"], k=w["k_new"],
+                                           v=w["v_new"], out=out, lse=lse, workspace=ws,
+                                           max_seqlen_k=ctx)
+            steps = max(5, min(200, int(2e9 / max(1, B * ctx * 16384))))
+            # cold cache: inputs below 4x L2 are timed with an L2 flush per call
+            by = algorithmic_bytes(B, ctx, 1, 1, 32, 32, 128)
+            if by < 4 * 129e6:
+                flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+                ts = []
+                for i in range(steps + 3):
+                    flush.zero_()
+                    # keep the stream busy while the host enqueues the call, so the
+                    # events bracket device time only
+                    torch.cuda._sleep(100000)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    e1.synchronize()
+                    if i >= 3:
+                        ts.append(e0.elapsed_time(e1) * 1e3)
+                us = statistics.median(ts)
+                mode = "cold (L2 flushed per call)"
+                del flush
+            else:
+                us = time_calls(fn, steps, 3, stream, graph=False)
+                mode = "inputs > 4x L2"
+            gbs = by / us / 1e3
+            ideal_us = by / (peak * 1e3)
+            print(json.dumps({"sweep": "paged decode", "ctx": ctx, "batch": B, "us": round(us, 2),
+                              "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
+                              "peak": peak, "peak_source": src, "timing": mode,
+                              "graded": ideal_us >= 20.0}), flush=True)
+            del w, out, lse, ws
+            torch.cuda.empty_cache()
+
+
 def secondary_measurements(dev, only=None):
     """Other configurations of the path, each timed alone with CUDA events
     (median-free mean over the timed calls, after warm-up)."""
@@ -437,6 +496,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the other configurations (prefill, GQA split-KV, tiny decode)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the paged decode sweep (ctx 512..4096 x batch 1..256) instead")
     ap.add_argument("--only", choices=["prefill", "gqa"],
                     help="time only this secondary leg (for profiling runs)")
     args = ap.parse_args()
@@ -464,6 +525,9 @@ def main():
     torch.cuda.set_device(dev)
     if args.only:
         print(json.dumps(secondary_measurements(dev, only=args.only)), flush=True)
+        return
+    if args.sweep:
+        decode_sweep(dev)
         return
     B, ctx, lnew = WORKLOAD["batch"], WORKLOAD["ctx"], WORKLOAD["lnew"]
     hq, hkv, d = WORKLOAD["num_q_heads"], WORKLOAD["num_kv_heads"], WORKLOAD["head_dim"]
