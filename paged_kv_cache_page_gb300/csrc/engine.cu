@@ -338,13 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c0 = 0, c1 = 0;
         if (b < p.B) {
           const SeqI q = seq_of(p, b, false);
+          int n = 0;
           if (packed_seq(p, q.qlen)) {
-            int n;
             packed_split(p, (q.lk + kPage - 1) / kPage, sc.chunk, &n);
             c1 = n * p.Hkv;
           } else if (q.qlen > 0) {
             c0 = ((q.qlen + kBM - 1) / kBM + 1) / 2 * p.Hq;
           }
+          // split count read by the combine step, for EVERY sequence: 0 for
+          // sequences written directly (unsplit, query tiles, empty entries)
+          if (blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
         }
         int i0 = c0, i1 = c1;
 #pragma unroll
@@ -615,8 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int vis_end = p.causal ? min(it.k1, qi + it.lk - it.qlen + 1) : it.k1;
       if (!valid) vis_end = it.k0;
       const bool to_partial = it.kind == 1 && it.nsplit > 1;
-      if (it.kind == 1 && it.split == 0 && it.head == 0 && tid == 0 && p.nsplit != nullptr)
-        p.nsplit[it.b] = to_partial ? it.nsplit : 0;
       const int64_t grow = it.row0 + qi;
       const int64_t nrows_all = p.cu_seqlens_q ? (int64_t)p.total_q : (int64_t)p.B * p.Lq;
       auto write_half = [&](const float* ov, int c, float inv) {  // 32 columns at hf*kDH + c*32

@@ -58,6 +58,23 @@ def test_split_count_does_not_change_result(splits):
     assert_close(out, lse, ref_o, ref_l, "f16")
 
 
+@pytest.mark.parametrize("hq,hkv,lq", [(8, 8, 1), (16, 2, 1), (8, 2, 4)])
+def test_stale_workspace_bytes(hq, hkv, lq):
+    """A workspace holding other bytes (split counts of 0x01010101, finite
+    partials) gives the same result: the CUDA-core decode (Lq*G <= 2) and the
+    packed tensor-core items (Lq*G > 2) rewrite every sequence's split count."""
+    lens = [900, 5, 2000, 4, 17, 600]
+    w = wl.paged_decode(len(lens), 0, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                        lens=lens, lnew=lq, seed=21 + hq + lq, device=DEV)
+    ref_o, ref_l = oracle_kvcache(w)
+    cap = w["block_table"].shape[1] * 16
+    nbytes = pa.fwd_kvcache_workspace_size(len(lens), lq, hq, hkv, 128, cap, 0)
+    assert nbytes > 0
+    ws = torch.full((nbytes,), 0x01, dtype=torch.uint8, device=DEV)
+    out, lse = run(w, workspace=ws)
+    assert_close(out, lse, ref_o, ref_l, "f16")
+
+
 def test_split_matches_unsplit_closely():
     w = wl.paged_decode(3, 2048, num_q_heads=4, num_kv_heads=4, seed=12, device=DEV)
     o1, l1 = run(w, num_splits=1)

@@ -14,14 +14,14 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def run(w):
+def run(w, workspace=None):
     err = pa.new_err_word(DEV)
     out = torch.full_like(w["q"], float("nan"))
     lse = torch.full((w["q"].shape[1], w["q"].shape[0]), float("nan"), device=DEV)
     pa.pa_fwd_varlen_unified(w["q"], w["k_cache"], w["v_cache"], w["cu_seqlens_q"],
                              w["seqlens_k"], w["block_table"], w["max_seqlen_q"],
                              w["max_seqlen_k"], scale=w["scale"], causal=w["causal"], out=out,
-                             lse=lse, err=err)
+                             lse=lse, err=err, workspace=workspace)
     torch.cuda.synchronize()
     assert err[0].item() == 0, err.tolist()
     return out, lse
@@ -72,3 +72,23 @@ def test_unified_zero_length_keys_and_single_key():
     cu = w["cu_seqlens_q"].cpu().tolist()
     assert torch.all(out[cu[1]] == 0) and torch.all(torch.isneginf(lse[:, cu[1]]))
     check(w, out, lse, "bf16", seqs=[0, 2, 3])
+
+
+@pytest.mark.parametrize("fill", [0x01, 0x3F])
+def test_unified_stale_workspace_bytes(fill):
+    """Every launch rewrites the per-sequence split counts that the combine
+    step reads, for every sequence (query-tile prefills and empty padding
+    entries included): a workspace still holding other bytes -- here a
+    constant byte, i.e. a split count of 0x01010101 or 0x3F3F3F3F and finite
+    partials -- changes no output."""
+    w = wl.unified_mixed(num_heads=16, num_kv_heads=4, head_dim=128, prefill_lens=(7, 40, 300),
+                         prefix_hi=700, num_decode=9, ctx_lo=1, ctx_hi=900, pad_to=16,
+                         device=DEV, seed=77)
+    total_q, hq, d = w["q"].shape
+    B = w["cu_seqlens_q"].numel() - 1
+    nbytes = pa.load_library().pa_fwd_varlen_workspace_size(
+        B, total_q, w["max_seqlen_q"], hq, w["k_cache"].shape[2], d, w["max_seqlen_k"])
+    assert nbytes > 0  # the batch is split: the combine step runs
+    ws = torch.full((nbytes,), fill, dtype=torch.uint8, device=DEV)
+    out, lse = run(w, workspace=ws)
+    check(w, out, lse, "bf16")
