@@ -9,9 +9,10 @@
 //
 // CTA = 1 producer warp + 4 consumer warps.  The producer resolves every
 // 16-token page absolutely from the block table (flash-attention #824 "Add
-// support for small page sizes": one page per fetch, resolved at the start of
-// each iteration; the relative page-delta bug discussed there cannot arise)
-// and issues one TMA box {D, 1 head, 16 tokens} per page for K and for V into
+// support for small page sizes": one page per fetch, each from its own table
+// entry; the relative page-delta bug discussed there cannot arise), reading
+// the entries warp-wide 32 at a time one batch ahead of use, and issues one
+// TMA box {D, 1 head, 16 tokens} per page for K and for V from eight lanes into
 // a 3-stage shared-memory ring.  Consumer warp w owns page w of a stage: QK^T
 // with 8 lanes per key (16-byte shared loads), fp32 online softmax in the
 // log2 domain, PV with each lane owning D/32 output columns.  The four warps'
@@ -154,6 +155,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
         if (b < p.B) {
           SeqInfo si = seq_info<RMAX>(p, b, false);
           if (si.active) split_pages_per(sch, (si.lk + kPage - 1) / kPage, chunk, &n);
+          // split count read by the combine step, for every sequence (0: the
+          // sequence's rows are written directly)
+          if (blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
         }
         int incl = n;
 #pragma unroll
@@ -205,53 +209,78 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
   const int num_ctas = gridDim.x;
 
   if (warp == Tr::kConsumerWarps) {
-    // ======================= producer =======================
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, p.k_sb, p.k_st};
-      int stage = 0;
-      uint32_t phase = 0;
-      bool failed = false;
-      for (int item = cta; item < num_items; item += num_ctas) {
-        int b, g, s, nb, p0, p1;
-        SeqInfo si;
-        item_of(item, b, g, s, nb, p0, p1, si);
-        for (int pg = p0; pg < p1; pg += Tr::kStagePages) {
-          if (!failed && !mbar_wait(&empty[stage], phase ^ 1)) {
-            report(p.err, PA_DEVERR_TIMEOUT, b, pg);
-            failed = true;
-          }
-          const int n = min(Tr::kStagePages, p1 - pg);
-          PageRef refs[Tr::kStagePages];
-#pragma unroll
-          for (int w = 0; w < Tr::kStagePages; ++w) {
-            if (w < n) {
-              refs[w] = resolve_page(geom, b, pg + w);
-              if (!refs[w].ok) report(p.err, PA_DEVERR_PAGE_OOB, b, pg + w);
-              int* info = sInfo + (stage * Tr::kStagePages + w) * 3;
-              info[0] = refs[w].c2;
-              info[1] = refs[w].c3;
-              info[2] = refs[w].ok ? 1 : 0;
-            }
-          }
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(n * 2 * Tr::kPageBytes));
-#pragma unroll
-          for (int w = 0; w < Tr::kStagePages; ++w) {
-            if (w < n) {
-              T* dk = sK + (stage * Tr::kStagePages + w) * Tr::kPageElems;
-              T* dv = sV + (stage * Tr::kStagePages + w) * Tr::kPageElems;
-              tma_load_4d(dk, &tmk, &full[stage], 0, g, refs[w].c2, refs[w].c3, pol);
-              tma_load_4d(dv, &tmv, &full[stage], 0, g, refs[w].c2, refs[w].c3, pol);
-            }
-          }
-          if (++stage == Tr::kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+    // ======================= producer warp =======================
+    // The block-table entries of the item are read warp-wide, one page per
+    // lane, 32 pages at a time and one batch ahead, so no stage waits on a
+    // table load.  Lanes 0-3 issue the K boxes and lanes 4-7 the V boxes of
+    // a stage's pages.
+    const uint64_t pol = l2_policy_evict_first();
+    CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, p.k_sb, p.k_st};
+    int stage = 0;
+    uint32_t phase = 0;
+    bool failed = false;
+    auto fetch = [&](int b, int lp, int p1, int& c2, int& c3, int& ok) {
+      c2 = 0;
+      c3 = 0;
+      ok = 0;
+      if (lp < p1) {
+        const PageRef r = resolve_page(geom, b, lp);
+        if (!r.ok) report(p.err, PA_DEVERR_PAGE_OOB, b, lp);
+        c2 = r.c2;
+        c3 = r.c3;
+        ok = r.ok ? 1 : 0;
+      }
+    };
+    for (int item = cta; item < num_items; item += num_ctas) {
+      int b, g, s, nb, p0, p1;
+      SeqInfo si;
+      item_of(item, b, g, s, nb, p0, p1, si);
+      int base = p0;
+      int cur2, cur3, curok, nxt2, nxt3, nxtok;
+      fetch(b, p0 + lane, p1, cur2, cur3, curok);
+      fetch(b, p0 + 32 + lane, p1, nxt2, nxt3, nxtok);
+      for (int pg = p0; pg < p1; pg += Tr::kStagePages) {
+        if (pg - base >= 32) {
+          base += 32;
+          cur2 = nxt2;
+          cur3 = nxt3;
+          curok = nxtok;
+          fetch(b, base + 32 + lane, p1, nxt2, nxt3, nxtok);
+        }
+        if (lane == 0 && !failed && !mbar_wait(&empty[stage], phase ^ 1)) {
+          report(p.err, PA_DEVERR_TIMEOUT, b, pg);
+          failed = true;
+        }
+        __syncwarp();
+        const int n = min(Tr::kStagePages, p1 - pg);
+        const int w = lane & (Tr::kStagePages - 1);
+        const int src = pg - base + w;
+        const int c2 = __shfl_sync(0xffffffffu, cur2, src);
+        const int c3 = __shfl_sync(0xffffffffu, cur3, src);
+        const int ok = __shfl_sync(0xffffffffu, curok, src);
+        if (lane < Tr::kStagePages && w < n) {
+          int* info = sInfo + (stage * Tr::kStagePages + w) * 3;
+          info[0] = c2;
+          info[1] = c3;
+          info[2] = ok;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(n * 2 * Tr::kPageBytes));
+        __syncwarp();
+        if (lane < 2 * Tr::kStagePages && w < n) {
+          const bool is_k = lane < Tr::kStagePages;
+          T* dst = (is_k ? sK : sV) + (stage * Tr::kStagePages + w) * Tr::kPageElems;
+          tma_load_4d(dst, is_k ? &tmk : &tmv, &full[stage], 0, g, c2, c3, pol);
+        }
+        if (++stage == Tr::kStages) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      // Drain: every issued stage must be consumed before this thread leaves,
-      // so no bulk copy can still target this CTA's shared memory.
+    }
+    // Drain: every issued stage must be consumed before the warp leaves, so
+    // no bulk copy can still target this CTA's shared memory.
+    if (lane == 0) {
       for (int i = 0; i < Tr::kStages; ++i) {
         if (!failed && !mbar_wait(&empty[stage], phase ^ 1)) failed = true;
         if (++stage == Tr::kStages) {
@@ -260,6 +289,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
         }
       }
     }
+    __syncwarp();
     return;
   }
 
@@ -468,8 +498,6 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
     named_barrier(1, Tr::kConsumerWarps * 32);
     if (warp == 0) {
       const bool to_partial = nb > 1;
-      if (to_partial && s == 0 && g == 0 && lane == 0 && p.nsplit != nullptr) p.nsplit[b] = nb;
-      if (!to_partial && s == 0 && g == 0 && lane == 0 && p.nsplit != nullptr) p.nsplit[b] = 0;
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         if (r < R) {
