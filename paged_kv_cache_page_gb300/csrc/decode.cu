@@ -7,17 +7,19 @@
 // replacement of a host num_splits heuristic, which would need the lengths on
 // the CPU: flash-attention #1000 "Inappropriate Number of Splits ...").
 //
-// CTA = 1 producer warp + 4 consumer warps.  The producer resolves every
+// CTA = 1 producer warp + 8 consumer warps.  The producer resolves every
 // 16-token page absolutely from the block table (flash-attention #824 "Add
 // support for small page sizes": one page per fetch, each from its own table
 // entry; the relative page-delta bug discussed there cannot arise), reading
 // the entries warp-wide 32 at a time one batch ahead of use, and issues one
 // TMA box {D, 1 head, 16 tokens} per page for K and for V from eight lanes into
-// a 3-stage shared-memory ring.  Consumer warp w owns page w of a stage: QK^T
-// with 8 lanes per key (16-byte shared loads), fp32 online softmax in the
-// log2 domain, PV with each lane owning D/32 output columns.  The four warps'
-// (m, l, O) are merged at the end of the item and written either as the final
-// output (one split) or as a normalised partial + LSE for the combine step.
+// a shared-memory ring of 4-page stages.  Consumer warps w and w + 4 own page w
+// of a stage, 8 keys each (two warps per page double the warps that hide the
+// latency of the per-key dependency chains): QK^T with 8 lanes per key
+// (16-byte shared loads), fp32 online softmax in the log2 domain, PV with each
+// lane owning D/32 output columns.  The eight warps' (m, l, O) are merged at
+// the end of the item and written either as the final output (one split) or
+// as a normalised partial + LSE for the combine step.
 //
 // New tokens of a kvcache call (k=/v= append) are patched into the staged page
 // from k_new/v_new and written to their cache slots by the CTA whose split
@@ -30,9 +32,11 @@ namespace {
 
 template <int D, typename T, int RMAX>
 struct DecodeTraits {
-  static constexpr int kConsumerWarps = 4;
+  static constexpr int kStagePages = 4;
+  static constexpr int kKeyParts = 2;  // consumer warps per page, 16 / kKeyParts keys each
+  static constexpr int kPartKeys = kPage / kKeyParts;
+  static constexpr int kConsumerWarps = kStagePages * kKeyParts;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
-  static constexpr int kStagePages = kConsumerWarps;
   static constexpr int kStages = (D == 128) ? 3 : 5;
   static constexpr int kPageElems = kPage * D;
   static constexpr int kPageBytes = kPageElems * 2;
@@ -93,7 +97,7 @@ __device__ __forceinline__ SeqInfo seq_info(const DecodeParams& p, int b, bool r
 }
 
 template <int D, typename T, int RMAX>
-__global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
+__global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
   using Tr = DecodeTraits<D, T, RMAX>;
@@ -299,6 +303,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
   bool failed = false;
   const int grp = lane >> 3;  // key slot within a QK pass
   const int sub = lane & 7;   // 16-byte chunk within the key row
+  const int slot = warp % Tr::kStagePages;  // page of the stage this warp reads
+  const int part = warp / Tr::kStagePages;  // which kPartKeys keys of that page
 
   for (int item = cta; item < num_items; item += num_ctas) {
     int b, g, s, nb, p0, p1;
@@ -352,20 +358,23 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
         report(p.err, PA_DEVERR_TIMEOUT, b, pg);
         failed = true;
       }
-      const int page = pg + warp;
+      const int page = pg + slot;
       if (page < p1) {
-        T* kp = sK + (stage * Tr::kStagePages + warp) * Tr::kPageElems;
-        T* vp = sV + (stage * Tr::kStagePages + warp) * Tr::kPageElems;
+        T* kp = sK + (stage * Tr::kStagePages + slot) * Tr::kPageElems;
+        T* vp = sV + (stage * Tr::kStagePages + slot) * Tr::kPageElems;
         const int t_base = page * kPage;
         const int nvalid = min(kPage, kend - t_base);
-        // New tokens of this page: patch the staged copy and append to the cache.
-        if (p.Lnew > 0 && t_base + nvalid > si.old) {
-          const int* info = sInfo + (stage * Tr::kStagePages + warp) * 3;
+        // New tokens among this warp's keys: patch the staged copy and append
+        // them to the cache (each warp patches only the rows it reads).
+        const int kb = part * Tr::kPartKeys;
+        if (p.Lnew > 0 && t_base + min(nvalid, kb + Tr::kPartKeys) > si.old) {
+          const int* info = sInfo + (stage * Tr::kStagePages + slot) * 3;
           const int c2 = info[0], c3 = info[1];
           const bool ok = info[2] != 0;
-          const int t0 = max(si.old - t_base, 0);
+          const int t0 = max(si.old - t_base, kb);
+          const int t1 = min(nvalid, kb + Tr::kPartKeys);
           constexpr int kChunks = D / 8;  // 16-byte chunks per row
-          for (int idx = lane; idx < (nvalid - t0) * kChunks; idx += 32) {
+          for (int idx = lane; idx < (t1 - t0) * kChunks; idx += 32) {
             const int t = t0 + idx / kChunks;
             const int c = idx % kChunks;
             const int64_t src = (((int64_t)b * p.Lnew + (t_base + t - si.old)) * p.Hkv + g) * D + c * 8;
@@ -386,11 +395,12 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
           __syncwarp();
         }
 
-        // ---- S = q K^T for the 16 keys of this page (4 passes of 4 keys)
-        float sc[RMAX][4];
+        // ---- S = q K^T for this warp's keys of the page (passes of 4 keys)
+        constexpr int kPasses = Tr::kPartKeys / 4;
+        float sc[RMAX][kPasses];
 #pragma unroll
-        for (int ps = 0; ps < 4; ++ps) {
-          const int t = ps * 4 + grp;
+        for (int ps = 0; ps < kPasses; ++ps) {
+          const int t = kb + ps * 4 + grp;
           const T* krow = kp + t * D;
           float kf[Tr::kQCh * 8];
 #pragma unroll
@@ -420,24 +430,28 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
           }
         }
         // ---- online softmax (log2 domain) and O += P V
-        float pr[RMAX][4];
+        float pr[RMAX][kPasses];
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
           if (r < R) {
-            float mx = fmaxf(fmaxf(sc[r][0], sc[r][1]), fmaxf(sc[r][2], sc[r][3]));
+            float mx = sc[r][0];
+#pragma unroll
+            for (int i = 1; i < kPasses; ++i) mx = fmaxf(mx, sc[r][i]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float mnew = fmaxf(m[r], mx);
             float alpha = 1.f;
             if (mnew == neg_inf()) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) pr[r][i] = 0.f;
+              for (int i = 0; i < kPasses; ++i) pr[r][i] = 0.f;
             } else {
               alpha = ex2(m[r] - mnew);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) pr[r][i] = ex2(sc[r][i] - mnew);
+              for (int i = 0; i < kPasses; ++i) pr[r][i] = ex2(sc[r][i] - mnew);
             }
-            float sum = (pr[r][0] + pr[r][1]) + (pr[r][2] + pr[r][3]);
+            float sum = pr[r][0];
+#pragma unroll
+            for (int i = 1; i < kPasses; ++i) sum += pr[r][i];
             sum += __shfl_xor_sync(0xffffffffu, sum, 8);
             sum += __shfl_xor_sync(0xffffffffu, sum, 16);
             l[r] = l[r] * alpha + sum;
@@ -447,9 +461,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 1)
           }
         }
 #pragma unroll
-        for (int t = 0; t < kPage; ++t) {
-          if (t < nvalid) {
-            const T* vrow = vp + t * D + lane * Tr::kPVE;
+        for (int t = 0; t < Tr::kPartKeys; ++t) {
+          if (kb + t < nvalid) {
+            const T* vrow = vp + (kb + t) * D + lane * Tr::kPVE;
             float vf[Tr::kPVE];
             if constexpr (Tr::kPVE == 4) {
               const uint2 u = *reinterpret_cast<const uint2*>(vrow);
@@ -600,8 +614,6 @@ cudaError_t launch_r(const DecodeParams& p, const CUtensorMap& tmk, const CUtens
   switch (rmax) {
     case 1: return launch_t<D, T, 1>(p, tmk, tmv, st);
     case 2: return launch_t<D, T, 2>(p, tmk, tmv, st);
-    case 4: return launch_t<D, T, 4>(p, tmk, tmv, st);
-    case 8: return launch_t<D, T, 8>(p, tmk, tmv, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -611,8 +623,6 @@ int occ_r(int rmax) {
   switch (rmax) {
     case 1: return occupancy_t<D, T, 1>();
     case 2: return occupancy_t<D, T, 2>();
-    case 4: return occupancy_t<D, T, 4>();
-    case 8: return occupancy_t<D, T, 8>();
   }
   return 0;
 }
