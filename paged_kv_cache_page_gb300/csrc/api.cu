@@ -341,7 +341,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
       c.total_q = 0;
       c.out = out;
       c.lse = lse;
-      e = launch_combine(c, D, dtype, B * Lq, st);
+      e = launch_combine(c, D, dtype, B * Lq, st, true);
       if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     }
     return PA_OK;
@@ -412,7 +412,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     c.total_q = 0;
     c.out = out;
     c.lse = lse;
-    e = launch_combine(c, D, dtype, B * Lq, st);
+    e = launch_combine(c, D, dtype, B * Lq, st, true);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
   return PA_OK;
@@ -499,7 +499,7 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
     c.total_q = total_q;
     c.out = out;
     c.lse = lse;
-    e = launch_combine(c, D, dtype, total_q, st);
+    e = launch_combine(c, D, dtype, total_q, st, true);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
   return PA_OK;

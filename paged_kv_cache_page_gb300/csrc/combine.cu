@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const CombineParams p, const long long rows_total) {
   using E = Elem<T>;
   constexpr int kPVE = D / 32;
+  // partials are complete once the producing grid has finished (a no-op when
+  // this launch does not depend on one programmatically)
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const long long w0 = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   const long long nwarps = (long long)gridDim.x * kCombineWarps;
@@ -93,24 +96,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 }
 
 template <int D, typename T>
-cudaError_t launch_t(const CombineParams& p, long long rows_total, cudaStream_t st) {
+cudaError_t launch_t(const CombineParams& p, long long rows_total, cudaStream_t st,
+                     bool dependent) {
   const long long warps = rows_total * p.Hq;
   long long blocks = (warps + kCombineWarps - 1) / kCombineWarps;
   const long long cap = 152LL * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  combine_kernel<D, T><<<(unsigned)blocks, kCombineWarps * 32, 0, st>>>(p, rows_total);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, T>, p, rows_total);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, int D, int dtype, int rows_total,
-                           cudaStream_t st) {
-  if (D == 128 && dtype == PA_F16) return launch_t<128, __half>(p, rows_total, st);
-  if (D == 128 && dtype == PA_BF16) return launch_t<128, __nv_bfloat16>(p, rows_total, st);
-  if (D == 64 && dtype == PA_F16) return launch_t<64, __half>(p, rows_total, st);
-  if (D == 64 && dtype == PA_BF16) return launch_t<64, __nv_bfloat16>(p, rows_total, st);
+                           cudaStream_t st, bool dependent) {
+  if (D == 128 && dtype == PA_F16) return launch_t<128, __half>(p, rows_total, st, dependent);
+  if (D == 128 && dtype == PA_BF16)
+    return launch_t<128, __nv_bfloat16>(p, rows_total, st, dependent);
+  if (D == 64 && dtype == PA_F16) return launch_t<64, __half>(p, rows_total, st, dependent);
+  if (D == 64 && dtype == PA_BF16)
+    return launch_t<64, __nv_bfloat16>(p, rows_total, st, dependent);
   return cudaErrorInvalidValue;
 }
 

@@ -52,7 +52,9 @@ struct DecodeTraits {
   static constexpr int kOffInfo = al16(kOffPrefix + (kDecodeMaxSchedB + 1) * 4);
   static constexpr int kOffBar = al16(kOffInfo + kStages * kStagePages * 12);
   static constexpr int kOffMisc = al16(kOffBar + 2 * kStages * 8);
-  static constexpr int kSmemBytes = ((kOffMisc + 64) + 127) & ~127;
+  static constexpr int kOffQ = kOffMisc + 64;  // [stage][RMAX][D] query rows of an item
+  static constexpr int kQRowBytes = D * 2;
+  static constexpr int kSmemBytes = ((kOffQ + kStages * RMAX * kQRowBytes) + 127) & ~127;
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(kOffV % 128 == 0, "TMA destinations need 128-byte alignment");
 };
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Tr::kOffBar);
   uint64_t* empty = full + Tr::kStages;
   int* sMisc = reinterpret_cast<int*>(smem + Tr::kOffMisc);
+  T* sQ = reinterpret_cast<T*>(smem + Tr::kOffQ);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -135,30 +138,78 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
   if (direct) {
     num_items = p.B * p.Hkv;
   } else {
-    // total page-heads (block reduction)
-    long long part = 0;
+    // pages of every sequence -> sPrefix (scratch until the prefix sum
+    // replaces it) and the longest one (block max); then the cost of each
+    // candidate split count (block sums of the work items it makes)
+    SplitSched sch{p.s_max, p.target_ctas, p.min_chunk_pages};
+    int* sRed = reinterpret_cast<int*>(sMerge);  // [warp][kSplitCands]
+    int pmax = 0;
     for (int b = tid; b < p.B; b += Tr::kThreads) {
       SeqInfo si = seq_info<RMAX>(p, b, true);
-      if (si.active) part += (si.lk + kPage - 1) / kPage;
+      const int pages = si.active ? (si.lk + kPage - 1) / kPage : -1;
+      sPrefix[b] = pages;
+      pmax = max(pmax, pages);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    long long* sRed = reinterpret_cast<long long*>(sMerge);
-    if (lane == 0) sRed[warp] = part;
+    for (int o = 16; o > 0; o >>= 1) pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
+    if (lane == 0) sRed[warp] = pmax;
     __syncthreads();
-    long long total = 0;
-    for (int w = 0; w < Tr::kThreads / 32; ++w) total += sRed[w];
-    SplitSched sch{p.s_max, p.target_ctas, p.min_chunk_pages};
-    chunk = split_chunk_pages(sch, total * p.Hkv, p.B, p.Hkv);
+    pmax = 0;
+    for (int w = 0; w < Tr::kThreads / 32; ++w) pmax = max(pmax, sRed[w]);
     __syncthreads();
+    if (p.target_ctas >= kForcedSplitTarget) {
+      chunk = max(1, p.min_chunk_pages);
+    } else {
+      int cchunk[kSplitCands], cnt[kSplitCands];
+#pragma unroll
+      for (int i = 0; i < kSplitCands; ++i) {
+        cchunk[i] = split_cand_chunk(sch, pmax, split_cand(i));
+        cnt[i] = 0;
+      }
+      for (int b = tid; b < p.B; b += Tr::kThreads) {
+        const int pages = sPrefix[b];
+        if (pages < 0) continue;
+#pragma unroll
+        for (int i = 0; i < kSplitCands; ++i) {
+          int n;
+          split_pages_per(sch, pages, cchunk[i], &n);
+          cnt[i] += n;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kSplitCands; ++i) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt[i] += __shfl_xor_sync(0xffffffffu, cnt[i], o);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kSplitCands; ++i) sRed[warp * kSplitCands + i] = cnt[i];
+      }
+      __syncthreads();
+      int best = -1;
+#pragma unroll
+      for (int i = 0; i < kSplitCands; ++i) {
+        const int n = split_cand(i);
+        if (n <= max(1, p.s_max)) {
+          int items = 0;
+          for (int w = 0; w < Tr::kThreads / 32; ++w) items += sRed[w * kSplitCands + i];
+          const int cost = split_cand_cost(sch, items * p.Hkv, cchunk[i], n > 1);
+          if (best < 0 || cost < best) {
+            best = cost;
+            chunk = cchunk[i];
+          }
+        }
+      }
+      __syncthreads();
+    }
     if (warp == 0) {
       int carry = 0;
       for (int base = 0; base < p.B; base += 32) {
         const int b = base + lane;
         int n = 0;
         if (b < p.B) {
-          SeqInfo si = seq_info<RMAX>(p, b, false);
-          if (si.active) split_pages_per(sch, (si.lk + kPage - 1) / kPage, chunk, &n);
+          const int pages = sPrefix[b];
+          if (pages >= 0) split_pages_per(sch, pages, chunk, &n);
           // split count read by the combine step, for every sequence (0: the
           // sequence's rows are written directly)
           if (blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
@@ -209,6 +260,9 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
     if (p0 > p1) p0 = p1;
   };
 
+  // the combine grid that follows may be scheduled now; it waits on the
+  // device for this grid's completion before reading any partial
+  griddep_launch_dependents();
   const int cta = blockIdx.x;
   const int num_ctas = gridDim.x;
 
@@ -269,8 +323,22 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
           info[2] = ok;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(n * 2 * Tr::kPageBytes));
+        // the item's query rows travel with its first stage
+        const int nq = (pg == p0) ? si.qlen * p.G : 0;
+        if (lane == 0)
+          mbar_arrive_expect_tx(&full[stage],
+                                (uint32_t)(n * 2 * Tr::kPageBytes + nq * Tr::kQRowBytes));
         __syncwarp();
+        if (lane < nq) {
+          const int qi = lane / p.G;
+          const int h = g * p.G + (lane % p.G);
+          const T* qrow =
+              p.cu_seqlens_q != nullptr
+                  ? reinterpret_cast<const T*>(p.q) + (si.row0 + qi) * p.q_st + (int64_t)h * p.q_sh
+                  : reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb + (int64_t)qi * p.q_st +
+                        (int64_t)h * p.q_sh;
+          bulk_load(sQ + (stage * RMAX + lane) * D, qrow, Tr::kQRowBytes, &full[stage]);
+        }
         if (lane < 2 * Tr::kStagePages && w < n) {
           const bool is_k = lane < Tr::kStagePages;
           T* dst = (is_k ? sK : sV) + (stage * Tr::kStagePages + w) * Tr::kPageElems;
@@ -313,36 +381,16 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
     const int R = si.qlen * p.G;  // <= RMAX for every item that exists
     const int kend = min(p1 * kPage, si.lk);
 
-    // q rows -> registers (pre-scaled into the log2 domain)
+    // q rows -> registers (pre-scaled into the log2 domain) once the item's
+    // first stage, which carries them, has landed
     float qf[RMAX][Tr::kQCh * 8];
     int lim[RMAX];
 #pragma unroll
     for (int r = 0; r < RMAX; ++r) {
       const int qi = r / p.G;
-      const int h = g * p.G + (r % p.G);
       lim[r] = p.causal ? qi + si.lk - si.qlen : 0x7fffffff;
-      if (r < R) {
-        const T* qrow;
-        if (p.cu_seqlens_q != nullptr)
-          qrow = reinterpret_cast<const T*>(p.q) + (si.row0 + qi) * p.q_st + (int64_t)h * p.q_sh;
-        else
-          qrow = reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb + (int64_t)qi * p.q_st +
-                 (int64_t)h * p.q_sh;
 #pragma unroll
-        for (int c = 0; c < Tr::kQCh; ++c) {
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + sub * 8));
-          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = E::to_f2(w4[e]);
-            qf[r][c * 8 + 2 * e] = f.x * p.scale_log2;
-            qf[r][c * 8 + 2 * e + 1] = f.y * p.scale_log2;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < Tr::kQCh * 8; ++e) qf[r][e] = 0.f;
-      }
+      for (int e = 0; e < Tr::kQCh * 8; ++e) qf[r][e] = 0.f;
     }
     float m[RMAX], l[RMAX], o[RMAX][Tr::kPVE];
 #pragma unroll
@@ -357,6 +405,25 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
       if (!failed && !mbar_wait(&full[stage], phase)) {
         report(p.err, PA_DEVERR_TIMEOUT, b, pg);
         failed = true;
+      }
+      if (pg == p0) {
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < R) {
+            const T* qrow = sQ + (stage * RMAX + r) * D;
+#pragma unroll
+            for (int c = 0; c < Tr::kQCh; ++c) {
+              const uint4 u = *reinterpret_cast<const uint4*>(qrow + c * 64 + sub * 8);
+              const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = E::to_f2(w4[e]);
+                qf[r][c * 8 + 2 * e] = f.x * p.scale_log2;
+                qf[r][c * 8 + 2 * e + 1] = f.y * p.scale_log2;
+              }
+            }
+          }
+        }
       }
       const int page = pg + slot;
       if (page < p1) {

@@ -377,6 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sc.total0 = misc[0];
     sc.total1 = misc[1];
   }
+  // the combine grid that follows may be scheduled now; it waits on the
+  // device for this grid's completion before reading any partial
+  griddep_launch_dependents();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();

@@ -114,6 +114,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Programmatic dependent launch: a grid lets the next (dependent) grid of its
+// stream be scheduled once all its CTAs have executed launch_dependents; the
+// dependent grid's griddep_wait returns when this grid has completed and its
+// memory writes are visible.  Both are no-ops without such a launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA / tensor core) accesses of the same locations.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -139,6 +150,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
       "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// Untiled bulk copy global -> shared, completing `bytes` on `bar`: both
+// addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -202,30 +222,47 @@ __device__ __forceinline__ PageRef resolve_page(const CacheGeom& g, int b, int l
 // host heuristic that would need the lengths on the CPU).  All CTAs of a
 // launch evaluate the same function of the same inputs, so they agree.
 //
-//   pages_b      = ceil(Lk_b / 16)
-//   total        = Hkv * sum_b pages_b       (page-heads of K/V to stream)
-//   chunk        = max(min_chunk, ceil(total / slots)), rounded up to 4 pages
-//   n_b          = clamp(ceil(pages_b / chunk), 1, s_max)
-//   per_b        = ceil(pages_b / n_b) rounded up to 4 pages; n_b = ceil(pages_b / per_b)
-// where slots = max(target_ctas - B*Hkv, target_ctas / 2) keeps the number
-// of work items near one wave of resident CTAs.
+//   pages_b   = ceil(Lk_b / 16),  P = max_b pages_b
+//   chunk(n)  = max(min_chunk, ceil(P / n) rounded up to 4 pages)
+//   n_b       = clamp(ceil(pages_b / chunk), 1, s_max)
+//   per_b     = ceil(pages_b / n_b) rounded up to 4 pages; n_b = ceil(pages_b / per_b)
+//   items(n)  = Hkv * sum_b n_b
+//   cost(n)   = ceil(items / target_ctas) * (chunk + 4) + (n > 1 ? 23 : 0)
+// and the candidate n in {1, 2, 3, 4, 6, 8, 12, 16} (<= s_max) of least cost
+// is taken: whole waves of resident CTAs times the pages one work item
+// streams, plus four pages' worth of fixed cost per item and 23 for the
+// partial writes and the combine step of a split (constants fitted to
+// measured paged-decode times over batch 1-64 and 1-4K keys on GB300).
+// With an explicit split count (target_ctas = 2^30, min_chunk = 1) every
+// sequence gets min(pages_b, s_max).
 struct SplitSched {
   int s_max;
   int target_ctas;
   int min_chunk_pages;
 };
 
+constexpr int kSplitCands = 8;
+constexpr int kForcedSplitTarget = 1 << 30;
+
 __device__ __forceinline__ int round_up4(int x) { return (x + 3) & ~3; }
 
-__device__ __forceinline__ int split_chunk_pages(const SplitSched& s, long long total_page_heads,
-                                                 int B, int Hkv) {
-  long long slots = (long long)s.target_ctas - (long long)B * Hkv;
-  if (slots < s.target_ctas / 2) slots = s.target_ctas / 2;
-  if (slots < 1) slots = 1;
-  long long c = (total_page_heads + slots - 1) / slots;
+__device__ __forceinline__ int split_cand(int i) {
+  return i < 4 ? i + 1 : (i == 4 ? 6 : i == 5 ? 8 : i == 6 ? 12 : 16);
+}
+
+// Chunk size (pages) of candidate split count n for a longest sequence of
+// `pmax` pages.
+__device__ __forceinline__ int split_cand_chunk(const SplitSched& s, int pmax, int n) {
+  int c = round_up4((pmax + n - 1) / n);
   if (c < s.min_chunk_pages) c = s.min_chunk_pages;
-  if (c > (1 << 28)) c = 1 << 28;
-  return round_up4((int)c);
+  return c < 4 ? 4 : c;
+}
+
+// Cost of a candidate in page-times, see above.
+__device__ __forceinline__ int split_cand_cost(const SplitSched& s, int items, int chunk,
+                                               bool split) {
+  const int waves = (items + s.target_ctas - 1) / s.target_ctas;
+  return waves * (chunk + 4) + (split ? 23 : 0);
 }
 
 // Pages per split for a sequence of `pages` pages; writes the split count.

@@ -75,8 +75,11 @@ struct AppendParams {
 // Launchers (each defined in the .cu file that holds its kernel).  They
 // return a cudaError_t from the launch.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+// `dependent`: launched as a programmatic dependent of the kernel just
+// enqueued on `st` (its blocks may be scheduled while that kernel drains and
+// wait on the device until it has completed and its writes are visible).
 cudaError_t launch_combine(const CombineParams& p, int D, int dtype, int rows_total,
-                           cudaStream_t st);
+                           cudaStream_t st, bool dependent = false);
 // Decode: `rmax` in {1,2,4,8}.  tmk/tmv are 4-D tensor maps of the caches
 // with box {D, 1, 16, 1}.
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
