@@ -502,6 +502,9 @@ def main():
                     help="time only this secondary leg (for profiling runs)")
     args = ap.parse_args()
     WORKLOAD["batch"], WORKLOAD["ctx"] = args.batch, args.ctx
+    kv_gb = args.batch * args.ctx * 32 * 128 * 2 * 2 / 1e9
+    WORKLOAD["l2"] = (f"inputs ({kv_gb:.1f} GB of K/V) larger than L2; no flush" if kv_gb > 4 * 0.129
+                      else f"inputs ({kv_gb:.2f} GB of K/V) within 4x L2")
     args.warmup = max(3, args.warmup)
     rank, world, local = dist_env()
 
