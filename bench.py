@@ -121,6 +121,37 @@ def time_calls(fn, steps, warmup, stream, graph=True):
     return e0.elapsed_time(e1) / steps * 1e3
 
 
+def mma_rate(dev):
+    """Back-to-back kind::f16 MMAs of M=128, K=16 on every SM (one CTA each):
+    cycles per instruction on the SM clock and the whole-GPU rate from CUDA
+    events, for the engine's shapes (N=128 keys for Q K^T, N=D=128 with P in
+    TMEM for P V) and for N=256."""
+    import ctypes
+
+    import torch
+
+    from paged_kv_cache_page_gb300 import build as pabuild
+
+    lib = ctypes.CDLL(pabuild.lib_path(pabuild.SELFTEST_LIB))
+    lib.pa_selftest_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_longlong),
+                                        ctypes.POINTER(ctypes.c_float)]
+    grid = torch.cuda.get_device_properties(dev).multi_processor_count
+    tpeak, tsrc = read_tensor_peak()
+    n = 4096
+    for N, ts in ((128, 0), (128, 1), (256, 0)):
+        cyc = (ctypes.c_longlong * 2)()
+        ms = ctypes.c_float()
+        rc = lib.pa_selftest_mma_rate(n, N, ts, grid, cyc, ctypes.byref(ms))
+        tf = 2.0 * 128 * N * 16 * n * grid / (ms.value * 1e-3) / 1e12 if rc == 0 else None
+        print(json.dumps({"mma_rate": f"M=128 N={N} K=16 kind::f16, A from {'TMEM' if ts else 'SMEM'}",
+                          "rc": rc, "instr_per_cta": n, "ctas": grid,
+                          "cycles_per_instr": round(cyc[1] / n, 1) if rc == 0 else None,
+                          "tflops": round(tf, 1) if tf else None,
+                          "frac_of_peak": round(tf / tpeak, 3) if tf else None,
+                          "peak": tpeak, "peak_source": tsrc}), flush=True)
+
+
 def decode_sweep(dev):
     """The paged decode sweep: ctx {512..4096} x batch {1..256}, 32 q = 32 kv
     heads, D 128, fp16, one appended token per sequence, automatic splits.
@@ -496,6 +527,9 @@ def main():
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the other configurations (prefill, GQA split-KV, tiny decode)")
+    ap.add_argument("--mma-rate", action="store_true",
+                    help="tensor-core rate of the M=128 MMA shapes the engine issues (N=128 SS, "
+                         "N=128 with A in TMEM) next to N=256; one JSON line each")
     ap.add_argument("--sweep", action="store_true",
                     help="time the paged decode sweep (ctx 512..4096 x batch 1..256) instead")
     ap.add_argument("--only", choices=["prefill", "gqa"],
@@ -528,6 +562,9 @@ def main():
     torch.cuda.set_device(dev)
     if args.only:
         print(json.dumps(secondary_measurements(dev, only=args.only)), flush=True)
+        return
+    if args.mma_rate:
+        mma_rate(dev)
         return
     if args.sweep:
         decode_sweep(dev)
