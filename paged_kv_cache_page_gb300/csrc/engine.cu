@@ -53,14 +53,12 @@ struct EngTraits {
   static constexpr int kStages = (D == 128) ? 2 : 3;
   static constexpr int kQBytes = kHalves * kSlab;
   static constexpr int kKVBytes = kHalves * kSlab;
-  static constexpr int kPBytes = 2 * kSlab;  // 128 keys
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffP = kOffV + kStages * kKVBytes;
-  static constexpr int kOffPre = kOffP + kPBytes;  // two int[kEngineMaxB + 1] prefix sums
+  static constexpr int kOffPre = kOffV + kStages * kKVBytes;  // two int[kEngineMaxB + 1] prefix sums
   static constexpr int kOffBar = kOffPre + ((2 * (kEngineMaxB + 1) * 4 + 15) & ~15);
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kOffX = (kOffBar + kNumBars * 8 + 15) & ~15;  // row max / sum exchange
   static constexpr int kOffMisc = kOffX + (2 * 2 * 128 + 128) * 4;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
@@ -255,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem + Tr::kOffQ;
   uint8_t* sK = smem + Tr::kOffK;
   uint8_t* sV = smem + Tr::kOffV;
-  uint8_t* sP = smem + Tr::kOffP;
   int* pre0 = reinterpret_cast<int*>(smem + Tr::kOffPre);
   int* pre1 = pre0 + (kEngineMaxB + 1);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::kOffBar);
@@ -267,9 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = k_empty + Tr::kStages;
   uint64_t* s_full = v_empty + Tr::kStages;  // [2]
   uint64_t* s_free = s_full + 2;             // [2]
+  // [2] by tile parity: with P in TMEM the softmax warps never wait for the
+  // previous P V, and they are synchronised only in pairs, so one lane quarter
+  // may arrive for tile j+1 before another has arrived for tile j
   uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* o_free = pv_done + 1;
+  uint64_t* pv_done = p_full + 2;  // [2]: P V of a tile of that parity completed
+  uint64_t* o_free = pv_done + 2;
   uint64_t* mma_fin = o_free + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Tr::kOffMisc);
   int* misc = reinterpret_cast<int*>(smem + Tr::kOffMisc + 16);
@@ -289,8 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], kSoftWarps);
     }
-    mbar_init(p_full, kSoftWarps);
-    mbar_init(pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], kSoftWarps);
+      mbar_init(&pv_done[i], 1);
+    }
     mbar_init(o_free, kSoftWarps);
     mbar_init(mma_fin, 1);
     fence_mbar_init();
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    long long* red = reinterpret_cast<long long*>(sP);  // P is free before the first tile
+    long long* red = reinterpret_cast<long long*>(sV);  // V is free before the first tile
     if (lane == 0) red[warp] = part;
     __syncthreads();
     long long total = 0;
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t id_qk = tc::idesc_f16(kBM, kBN, bf, false);
     const uint32_t id_pv = tc::idesc_f16(kBM, D, bf, true);
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP);
+    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int Tj = tctr + j;
         if (j + 1 < it.ntiles) issue_qk(j + 1);
         const int s = Tj % Tr::kStages;
-        wait(p_full, (uint32_t)(Tj & 1), 300);
+        wait(&p_full[Tj & 1], (uint32_t)((Tj >> 1) & 1), 300);
         wait(&v_full[s], (uint32_t)((Tj / Tr::kStages) & 1), 400);
         if (j == 0 && a >= 1) wait(o_free, (uint32_t)((a - 1) & 1), 450);
         // keys past the item's range: zero their V rows so P = 0 never meets a
@@ -565,13 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         if (lane == 0) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint32_t offp = (kk >> 2) * Tr::kSlab + (kk & 3) * 32;
-            tc::mma_f16_ss(tO, tc::smem_desc(aP + offp, 16, 1024),
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc::mma_f16_ts(tO, tS[Tj & 1] + kk * 8,
                            tc::smem_desc(aV + s * Tr::kKVBytes + kk * 2048, Tr::kSlab, 1024),
                            id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc::commit(pv_done);
+          tc::commit(&pv_done[Tj & 1]);
           tc::commit(&v_empty[s]);
         }
         __syncwarp();
@@ -696,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_before_sync();
         pair_sync();
+        tc::fence_after_sync();  // the partner's S loads precede this half's P stores
         if (quarter_live) mx = fmaxf(mx, xmax[((Tj & 1) * 2 + (hf ^ 1)) * 128 + r]);
         // both halves of a row see the same maximum and decide alike
         const float m_new = fmaxf(m_use, mx);
@@ -709,35 +710,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           m_use = m_new;
         }
-        // P buffer and O are free / stable once PV of the previous tile is done
-        if (Tj >= 1) wait(pv_done, (uint32_t)((Tj - 1) & 1), 600);
+        // P (16-bit) goes into TMEM over this tile's S: the row's 64 keys of
+        // this half -> columns [32 hf, 32 hf + 32) of the S buffer (both halves
+        // of the row loaded their S before the exchange above).  P V of the
+        // tile two back, which read the previous P there, was issued before the
+        // Q K^T that wrote this S, so no wait is needed.
         if (quarter_live) {
-          uint8_t* prow = sP + hf * Tr::kSlab + r * 128;
           const float neg_m = -m_use;
           float rs8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
-          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float e0 = ex2(fmaf(v[2 * i], sc_l2, neg_m));
-            float e1 = ex2(fmaf(v[2 * i + 1], sc_l2, neg_m));
-            if (!full) {
-              e0 = (2 * i < lim) ? e0 : 0.f;
-              e1 = (2 * i + 1 < lim) ? e1 : 0.f;
+          for (int q2 = 0; q2 < 2; ++q2) {  // 16 columns (32 keys) per store
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k = q2 * 32 + 2 * i;
+              float e0 = ex2(fmaf(v[k], sc_l2, neg_m));
+              float e1 = ex2(fmaf(v[k + 1], sc_l2, neg_m));
+              if (!full) {
+                e0 = (k < lim) ? e0 : 0.f;
+                e1 = (k + 1 < lim) ? e1 : 0.f;
+              }
+              rs8[i & 7] += e0 + e1;
+              pk[i] = E::from_f2(e0, e1);
             }
-            rs8[i & 7] += e0 + e1;
-            pk[i] = E::from_f2(e0, e1);
+            tc::tmem_st16u(tS[Tj & 1] + lane_off + hf * 32 + q2 * 16, pk);
           }
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
-                make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
           l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[Tj & 1]);
         if (j >= 1 && quarter_live && __any_sync(0xffffffffu, rescale)) {
+          // O is stable once P V of the previous tile is done
+          wait(&pv_done[(Tj - 1) & 1], (uint32_t)(((Tj - 1) >> 1) & 1), 650);
+          tc::fence_after_sync();
           const float sa = rescale ? alpha : 1.f;
 #pragma unroll 1
           for (int c = 0; c < kDH / 32; ++c) {
@@ -749,12 +754,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) ov[i] *= sa;
             tc::tmem_st32(ta, ov);
           }
-          tc::tmem_wait_st();
         }
-        fence_proxy_async_smem();
+        tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) {
+          mbar_arrive(&s_free[Tj & 1]);
+          mbar_arrive(&p_full[Tj & 1]);
+        }
       }
       // ---- epilogue: the two halves' sums, then O / l and LSE
       if (hf == 1) xl[r] = l;
@@ -762,7 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (hf == 0) xl[r] = l + xl[r];
       pair_sync();
       const float L = xl[r];
-      wait(pv_done, (uint32_t)((tctr + it.ntiles - 1) & 1), 700);
+      {
+        const int tl = tctr + it.ntiles - 1;
+        wait(&pv_done[tl & 1], (uint32_t)((tl >> 1) & 1), 700);
+      }
       tc::fence_after_sync();
       const float inv = L > 0.f ? 1.f / L : 0.f;
       if (quarter_live) {
