@@ -134,17 +134,18 @@ def mma_rate(dev):
 
     lib = ctypes.CDLL(pabuild.lib_path(pabuild.SELFTEST_LIB))
     lib.pa_selftest_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                        ctypes.POINTER(ctypes.c_longlong),
+                                        ctypes.c_int, ctypes.POINTER(ctypes.c_longlong),
                                         ctypes.POINTER(ctypes.c_float)]
     grid = torch.cuda.get_device_properties(dev).multi_processor_count
     tpeak, tsrc = read_tensor_peak()
     n = 4096
-    for N, ts in ((128, 0), (128, 1), (256, 0)):
+    for N, ts, ks in ((128, 0, 4), (128, 0, 8), (128, 1, 4), (128, 1, 8), (256, 0, 4), (256, 0, 8)):
         cyc = (ctypes.c_longlong * 2)()
         ms = ctypes.c_float()
-        rc = lib.pa_selftest_mma_rate(n, N, ts, grid, cyc, ctypes.byref(ms))
+        rc = lib.pa_selftest_mma_rate(n, N, ts, ks, grid, cyc, ctypes.byref(ms))
         tf = 2.0 * 128 * N * 16 * n * grid / (ms.value * 1e-3) / 1e12 if rc == 0 else None
         print(json.dumps({"mma_rate": f"M=128 N={N} K=16 kind::f16, A from {'TMEM' if ts else 'SMEM'}",
+                          "ksteps": ks,
                           "rc": rc, "instr_per_cta": n, "ctas": grid,
                           "cycles_per_instr": round(cyc[1] / n, 1) if rc == 0 else None,
                           "tflops": round(tf, 1) if tf else None,
