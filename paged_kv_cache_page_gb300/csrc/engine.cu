@@ -14,18 +14,20 @@
 // A varlen batch may mix both kinds in one launch: the unified launch of vLLM
 // #6052 "Unify the kernel used in flash attention backend".
 //
-// CTA = 320 threads, one per SM, persistent over items:
+// CTA = 416 threads, one per SM, persistent over items:
 //   warps 0-7  softmax: warps w and w+4 share tile rows 32(w%4).. (their TMEM
 //              lane quarter), each taking 64 of the 128 columns.  S from TMEM,
 //              masking, running max / sum in the log2 domain, P (fp16/bf16)
 //              to shared memory in the 128-byte-swizzled K-major layout, lazy
 //              O rescale (only when the max grows by more than 2^8), epilogue.
-//   warp 8     TMA producer: Q of the item, then per 128-key tile 8 pages of K
-//              and V, each page resolved absolutely from the block table.
-//   warp 9     TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
-//              buffers (tile j+1 issued before P V of tile j), O += P V.
-// TMEM: S0 cols [0,128), S1 [128,256), O [256, 256+D).  Pipeline state
-// (stage and buffer parities) runs on across items.
+//   warps 8-11 TMA producers: Q of the item, then per 128-key tile 8 pages of
+//              K and V (each warp a quarter of the page boxes), each page
+//              resolved absolutely from the block table.
+//   warp 12    TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
+//              buffers (tile j+1 issued before P V of tile j), O += P V with P
+//              read from TMEM.
+// TMEM: S0 (then P0) cols [0,128), S1 (then P1) [128,256), O [256, 256+D).
+// Pipeline state (stage and buffer parities) runs on across items.
 #include <type_traits>
 
 #include "pa_common.cuh"
