@@ -43,3 +43,29 @@ def test_tcgen05_operand_layouts(dtype, d, a_col):
     torch.testing.assert_close(C1, ref1, rtol=1e-4, atol=1e-3)
     torch.testing.assert_close(C2, ref2, rtol=1e-4, atol=1e-3)
     torch.testing.assert_close(C3, ref2, rtol=1e-4, atol=1e-3)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_tcgen05_transposed_decode_shapes(dtype):
+    """The transposed decode-tile shapes: C4 = K Q^T with N = 16 query rows
+    (both operands K-major, fetched by TMA) and C5 = V^T P^T with the V tile
+    read as an MN-major A operand and a 16-row P tile written by threads."""
+    pabuild.build()
+    lib = ctypes.CDLL(pabuild.lib_path(pabuild.SELFTEST_LIB))
+    g = torch.Generator(device=DEV).manual_seed(7)
+    K = torch.randn((128, 128), generator=g, device=DEV).to(dtype)
+    Q = torch.randn((128, 128), generator=g, device=DEV).to(dtype)
+    V = torch.randn((128, 128), generator=g, device=DEV).to(dtype)
+    P = torch.randn((16, 128), generator=g, device=DEV).to(dtype)
+    C4 = torch.full((128, 16), float("nan"), device=DEV)
+    C5 = torch.full((128, 16), float("nan"), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    rc = lib.pa_selftest_tcgen05_transposed(p(K), p(Q), p(V), p(P), p(C4), p(C5),
+                                            pa.PA_BF16 if dtype == torch.bfloat16 else pa.PA_F16,
+                                            p(status),
+                                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == 0 and status.item() == 0
+    torch.testing.assert_close(C4, K.float() @ Q[:16].float().T, rtol=1e-4, atol=1e-3)
+    torch.testing.assert_close(C5, V.float().T @ P.float().T, rtol=1e-4, atol=1e-3)
