@@ -57,6 +57,36 @@ int plan_s_max(int B, int Hkv, int max_seqlen_k, int num_splits) {
   return std::max(1, s);
 }
 
+// Would the device split schedule (split-KV schedule in pa_common.cuh) split
+// anything for B sequences of the capacity max_seqlen_k?  The same candidate
+// costs, evaluated on the host for uniform lengths at that bound: when even
+// then one split per sequence wins, the call runs unsplit (no schedule, no
+// combine launch), which is what the device would choose for lengths at the
+// bound and costs at most the split gain of shorter, ragged batches.
+bool decode_splits_useful(int B, int Hkv, int max_seqlen_k, int s_max, int target_ctas) {
+  if (s_max <= 1 || target_ctas < 1) return false;
+  const int P = std::max(1, (max_seqlen_k + kPage - 1) / kPage);
+  const int cands[8] = {1, 2, 3, 4, 6, 8, 12, 16};
+  auto up4 = [](int x) { return (x + 3) & ~3; };
+  long long best = -1;
+  int best_n = 1;
+  for (int n : cands) {
+    if (n > s_max) break;
+    int c = up4((P + n - 1) / n);
+    c = std::max(std::max(c, kMinChunkPages), 4);
+    int k = std::min(std::max(1, (P + c - 1) / c), s_max);  // splits of a P-page sequence
+    const int per = up4((P + k - 1) / k);
+    k = (P + per - 1) / per;
+    const long long items = (long long)B * Hkv * k;
+    const long long cost = (items + target_ctas - 1) / target_ctas * (c + 4) + (n > 1 ? 23 : 0);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_n = k;
+    }
+  }
+  return best_n > 1;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct SplitWorkspace {
@@ -348,7 +378,9 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   }
 
   const int rmax = rows_template(rows);
-  const int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
+  const int resident = decode_resident_ctas(D, dtype, rmax);
+  int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
+  if (num_splits == 0 && !decode_splits_useful(B, Hkv, max_seqlen_k, s_max, resident)) s_max = 1;
   const SplitWorkspace ws = split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max);
   if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
@@ -389,7 +421,6 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
   p.s_max = s_max;
-  const int resident = decode_resident_ctas(D, dtype, rmax);
   p.target_ctas = num_splits > 0 ? (1 << 30) : resident;
   p.grid_ctas = resident;
   p.min_chunk_pages = num_splits > 0 ? 1 : kMinChunkPages;
