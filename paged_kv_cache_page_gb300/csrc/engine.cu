@@ -60,7 +60,12 @@ struct EngTraits {
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffPre = kOffV + kStages * kKVBytes;  // two int[kEngineMaxB + 1] prefix sums
   static constexpr int kOffBar = kOffPre + ((2 * (kEngineMaxB + 1) * 4 + 15) & ~15);
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 1 + 1;
+  // With two stages a K stage is free exactly when Q K^T of the tile two back
+  // has completed, which s_full of that parity already signals; likewise a V
+  // stage and pv_done.  The producers then wait on those, and the MMA thread
+  // saves two commits per tile.
+  static constexpr bool kSharedEmpty = kStages == 2;
   static constexpr int kOffX = (kOffBar + kNumBars * 8 + 15) & ~15;  // row max / sum exchange
   static constexpr int kOffMisc = kOffX + (2 * 2 * 128 + 128) * 4;
   static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
@@ -265,11 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = v_full + Tr::kStages;
   uint64_t* v_empty = k_empty + Tr::kStages;
   uint64_t* s_full = v_empty + Tr::kStages;  // [2]
-  uint64_t* s_free = s_full + 2;             // [2]
   // [2] by tile parity: with P in TMEM the softmax warps never wait for the
   // previous P V, and they are synchronised only in pairs, so one lane quarter
-  // may arrive for tile j+1 before another has arrived for tile j
-  uint64_t* p_full = s_free + 2;
+  // may arrive for tile j+1 before another has arrived for tile j.  It also
+  // tells the MMA thread that S of the tile is no longer read: Q K^T of tile
+  // j+2 is issued only after P V of tile j, which waited for p_full of j.
+  uint64_t* p_full = s_full + 2;
   uint64_t* pv_done = p_full + 2;  // [2]: P V of a tile of that parity completed
   uint64_t* o_free = pv_done + 2;
   uint64_t* mma_fin = o_free + 1;
@@ -282,15 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int i = 0; i < Tr::kStages; ++i) {
-      mbar_init(&k_full[i], kProdWarps);
-      mbar_init(&v_full[i], kProdWarps);
+      mbar_init(&k_full[i], kProdWarps / 2);
+      mbar_init(&v_full[i], kProdWarps / 2);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftWarps);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], kSoftWarps);
       mbar_init(&pv_done[i], 1);
@@ -394,9 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kWarpTMA && warp < kWarpMMA) {
     // ======================= TMA producers =======================
-    // kProdWarps warps run the same loop and split every tile's page boxes
-    // round-robin (TMA issue throughput grows with the number of issuing
-    // warps); each arrives on the stage barrier with its share of the bytes.
+    // Warps 0 and 1 of the group load K tiles, warps 2 and 3 V tiles, each
+    // taking alternate pages of every tile (TMA issue throughput grows with
+    // the number of issuing warps) and arriving on the stage barrier with its
+    // share of the bytes.  K and V run independently: a K stage is refilled as
+    // soon as Q K^T has read it, without waiting behind the V stage, which
+    // frees only after P V at the end of the tile's chain.
     // Within a warp:  Block-table entries are loaded 32 pages
     // (4 KV tiles) at a time, one lane per page, a batch ahead of use and with
     // no dependent instruction until the tile is issued, so the table reads
@@ -406,6 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_q = l2_policy_evict_first();
     const bool paged = p.block_table != nullptr;
     const int pw = warp - kWarpTMA;
+    const bool is_v = pw >= kProdWarps / 2;
+    const int sub = pw % (kProdWarps / 2);
+    uint64_t* x_full = is_v ? v_full : k_full;
+    uint64_t* x_empty = Tr::kSharedEmpty ? (is_v ? pv_done : s_full) : (is_v ? v_empty : k_empty);
+    uint8_t* sX = is_v ? sV : sK;
+    const CUtensorMap* tm_x = is_v ? &tm_v : &tm_k;
     bool failed = false;
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
@@ -465,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i < npg && !ok && lane == 0 && pw == 0) report(p.err, PA_DEVERR_PAGE_OOB, it.b, lp);
         }
         // box b = page (b % 8), 64-column slab (b / 8); this warp issues the
-        // boxes b = pw + kProdWarps * lane
-        const int my_box = pw + kProdWarps * lane;
+        // boxes b = sub + 2 * lane of its tensor
+        const int my_box = sub + 2 * lane;
         const int my_page = my_box & (kTilePages - 1);
         const int my_slab = my_box / kTilePages;
         const bool issuer = my_slab < Tr::kHalves && my_page < npg;
@@ -479,28 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mc3 = c3[i];
           }
         if (lane == 0) {
-          if (!failed && !mbar_wait(&k_empty[s], par ^ 1)) {
+          if (!failed && !mbar_wait(&x_empty[s], par ^ 1)) {
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
-          mbar_arrive_expect_tx(&k_full[s], (uint32_t)(my_count * 2048));
+          mbar_arrive_expect_tx(&x_full[s], (uint32_t)(my_count * 2048));
         }
         __syncwarp();
         if (issuer)
-          tma_load_4d(sK + s * Tr::kKVBytes + my_slab * Tr::kSlab + my_page * 2048, &tm_k,
-                      &k_full[s], my_slab * 64, g, mc2, mc3, pol_kv);
-        __syncwarp();
-        if (lane == 0) {
-          if (!failed && !mbar_wait(&v_empty[s], par ^ 1)) {
-            report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
-            failed = true;
-          }
-          mbar_arrive_expect_tx(&v_full[s], (uint32_t)(my_count * 2048));
-        }
-        __syncwarp();
-        if (issuer)
-          tma_load_4d(sV + s * Tr::kKVBytes + my_slab * Tr::kSlab + my_page * 2048, &tm_v,
-                      &v_full[s], my_slab * 64, g, mc2, mc3, pol_kv);
+          tma_load_4d(sX + s * Tr::kKVBytes + my_slab * Tr::kSlab + my_page * 2048, tm_x,
+                      &x_full[s], my_slab * 64, g, mc2, mc3, pol_kv);
         __syncwarp();
       }
       tctr += it.ntiles;
@@ -518,7 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool bf = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t id_qk = tc::idesc_f16(kBM, kBN, bf, false);
     const uint32_t id_pv = tc::idesc_f16(kBM, D, bf, true);
-    const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+    // Descriptor bases, built once: a tile's operands sit at fixed offsets
+    // from them, added to the start-address field (addr >> 4, 14 bits, never
+    // carried out of the field since shared memory is below 256 KB).  The
+    // issuing thread shares its scheduler with softmax warps, so every
+    // instruction spent per MMA lengthens the tile.
+    const uint64_t dQ = tc::smem_desc(smem_u32(sQ), 16, 1024);
+    const uint64_t dK0 = tc::smem_desc(smem_u32(sK), 16, 1024);
+    const uint64_t dV0 = tc::smem_desc(smem_u32(sV), Tr::kSlab, 1024);
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
@@ -527,17 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int Tq = tctr + jq;
         const int s = Tq % Tr::kStages;
         wait(&k_full[s], (uint32_t)((Tq / Tr::kStages) & 1), 100);
-        if (Tq >= 2) wait(&s_free[Tq & 1], (uint32_t)(((Tq - 2) >> 1) & 1), 200);
         tc::fence_after_sync();
         if (lane == 0) {
+          const uint64_t dK = dK0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
+          const uint32_t tSq = tS[Tq & 1];
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * Tr::kSlab + (kk & 3) * 32;
-            tc::mma_f16_ss(tS[Tq & 1], tc::smem_desc(aQ + off, 16, 1024),
-                           tc::smem_desc(aK + s * Tr::kKVBytes + off, 16, 1024), id_qk, kk > 0);
+            const uint32_t off = ((kk >> 2) * Tr::kSlab + (kk & 3) * 32) >> 4;
+            tc::mma_f16_ss(tSq, dQ + off, dK + off, id_qk, kk > 0);
           }
           tc::commit(&s_full[Tq & 1]);
-          tc::commit(&k_empty[s]);
+          if (!Tr::kSharedEmpty) tc::commit(&k_empty[s]);
           if (jq == it.ntiles - 1) tc::commit(q_empty);  // Q no longer read
         }
         __syncwarp();
@@ -548,8 +555,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int Tj = tctr + j;
         if (j + 1 < it.ntiles) issue_qk(j + 1);
         const int s = Tj % Tr::kStages;
-        wait(&p_full[Tj & 1], (uint32_t)((Tj >> 1) & 1), 300);
-        wait(&v_full[s], (uint32_t)((Tj / Tr::kStages) & 1), 400);
+        {
+          const uint32_t pp = (uint32_t)((Tj >> 1) & 1), pv = (uint32_t)((Tj / Tr::kStages) & 1);
+          if (failed || !mbar_try_wait2(&p_full[Tj & 1], pp, &v_full[s], pv)) {
+            wait(&p_full[Tj & 1], pp, 300);
+            wait(&v_full[s], pv, 400);
+          }
+        }
         if (j == 0 && a >= 1) wait(o_free, (uint32_t)((a - 1) & 1), 450);
         // keys past the item's range: zero their V rows so P = 0 never meets a
         // stale or non-finite value
@@ -568,13 +580,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         if (lane == 0) {
+          const uint64_t dV = dV0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
+          const uint32_t tP = tS[Tj & 1];
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            tc::mma_f16_ts(tO, tS[Tj & 1] + kk * 8,
-                           tc::smem_desc(aV + s * Tr::kKVBytes + kk * 2048, Tr::kSlab, 1024),
-                           id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_f16_ts(tO, tP + kk * 8, dV + (kk * 2048 >> 4), id_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
           tc::commit(&pv_done[Tj & 1]);
-          tc::commit(&v_empty[s]);
+          if (!Tr::kSharedEmpty) tc::commit(&v_empty[s]);
         }
         __syncwarp();
       }
@@ -761,7 +774,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&s_free[Tj & 1]);
           mbar_arrive(&p_full[Tj & 1]);
         }
       }

@@ -103,6 +103,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Both tests in one block, so that the second is issued before the first
+// returns: one round trip instead of two when both phases are complete.
+__device__ __forceinline__ bool mbar_try_wait2(uint64_t* bar0, uint32_t parity0, uint64_t* bar1,
+                                               uint32_t parity1) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+      "and.pred p, p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar0)), "r"(parity0), "r"(smem_u32(bar1)), "r"(parity1)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // (and never blocks longer than kWaitTimeoutNs) if it does not.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
