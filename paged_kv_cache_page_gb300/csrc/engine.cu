@@ -18,14 +18,14 @@
 //   warps 0-7  softmax: warps w and w+4 share tile rows 32(w%4).. (their TMEM
 //              lane quarter), each taking 64 of the 128 columns.  S from TMEM,
 //              masking, running max / sum in the log2 domain, P (fp16/bf16)
-//              to shared memory in the 128-byte-swizzled K-major layout, lazy
-//              O rescale (only when the max grows by more than 2^8), epilogue.
-//   warps 8-11 TMA producers: Q of the item, then per 128-key tile 8 pages of
-//              K and V (each warp a quarter of the page boxes), each page
+//              written back over S in TMEM, lazy O rescale (only when the max
+//              grows by more than 2^8), epilogue.
+//   warps 8-11 TMA producers: Q of the item (warp 8), then per 128-key tile
+//              8 pages of K (warps 8-9) and of V (warps 10-11), each page
 //              resolved absolutely from the block table.
-//   warp 12    TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
-//              buffers (tile j+1 issued before P V of tile j), O += P V with P
-//              read from TMEM.
+//   warp 12    TMEM owner and P V issuer: O += P V with P read from TMEM.
+//   warp 13    Q K^T issuer: S into one of two TMEM buffers, tile t once P V of
+//              tile t-2 (whose P occupies the buffer) has completed.
 // TMEM: S0 (then P0) cols [0,128), S1 (then P1) [128,256), O [256, 256+D).
 // Pipeline state (stage and buffer parities) runs on across items.
 #include <type_traits>
@@ -45,8 +45,9 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
 constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
 constexpr int kWarpTMA = kSoftWarps;        // first TMA producer warp
-constexpr int kWarpMMA = kSoftWarps + kProdWarps;  // MMA issuer + TMEM owner
-constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;
+constexpr int kWarpMMA = kSoftWarps + kProdWarps;  // P V issuer + TMEM owner
+constexpr int kWarpQK = kWarpMMA + 1;               // Q K^T issuer
+constexpr int kThreads = (kSoftWarps + kProdWarps + 2) * 32;
 
 template <int D>
 struct EngTraits {
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(o_free, kSoftWarps);
-    mbar_init(mma_fin, 1);
+    mbar_init(mma_fin, 2);  // one commit from each MMA issuer
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -506,8 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tctr += it.ntiles;
       ++a;
     }
-  } else if (warp == kWarpMMA) {
-    // ======================= MMA issuer =======================
+  } else if (warp == kWarpMMA || warp == kWarpQK) {
+    // ======================= MMA issuers =======================
+    // Warp 13 issues every S = Q K^T, warp 12 every O += P V, each from its
+    // lane 0 and each committing its own instructions.  Split in two, each
+    // issuer's chain of barrier round trips and commits per tile is half as
+    // long, and the two chains overlap.  Q K^T of tile t writes the TMEM
+    // buffer that holds P of tile t-2, so it waits for P V of that tile.
     bool failed = false;
     auto wait = [&](uint64_t* bar, uint32_t par, int where) {
       if (!failed && !mbar_wait(bar, par)) {
@@ -526,75 +532,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dQ = tc::smem_desc(smem_u32(sQ), 16, 1024);
     const uint64_t dK0 = tc::smem_desc(smem_u32(sK), 16, 1024);
     const uint64_t dV0 = tc::smem_desc(smem_u32(sV), Tr::kSlab, 1024);
+    const bool is_qk = warp == kWarpQK;
+    auto kv_par = [](int t) { return (uint32_t)((t / Tr::kStages) & 1); };
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
-      auto issue_qk = [&](int jq) {
-        const int Tq = tctr + jq;
-        const int s = Tq % Tr::kStages;
-        wait(&k_full[s], (uint32_t)((Tq / Tr::kStages) & 1), 100);
-        tc::fence_after_sync();
-        if (lane == 0) {
-          const uint64_t dK = dK0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
-          const uint32_t tSq = tS[Tq & 1];
+      if (is_qk) {
+        wait(q_full, (uint32_t)(a & 1), 50);
+        for (int j = 0; j < it.ntiles; ++j) {
+          const int Tq = tctr + j;
+          const int s = Tq % Tr::kStages;
+          if (Tq >= 2) {
+            const uint32_t pd = (uint32_t)(((Tq - 2) >> 1) & 1);
+            if (failed || !mbar_try_wait2(&k_full[s], kv_par(Tq), &pv_done[Tq & 1], pd)) {
+              wait(&k_full[s], kv_par(Tq), 100);
+              wait(&pv_done[Tq & 1], pd, 200);
+            }
+          } else {
+            wait(&k_full[s], kv_par(Tq), 100);
+          }
+          tc::fence_after_sync();
+          if (lane == 0) {
+            const uint64_t dK = dK0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
+            const uint32_t tSq = tS[Tq & 1];
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * Tr::kSlab + (kk & 3) * 32) >> 4;
-            tc::mma_f16_ss(tSq, dQ + off, dK + off, id_qk, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * Tr::kSlab + (kk & 3) * 32) >> 4;
+              tc::mma_f16_ss(tSq, dQ + off, dK + off, id_qk, kk > 0);
+            }
+            tc::commit(&s_full[Tq & 1]);
+            if (!Tr::kSharedEmpty) tc::commit(&k_empty[s]);
+            if (j == it.ntiles - 1) tc::commit(q_empty);  // Q no longer read
           }
-          tc::commit(&s_full[Tq & 1]);
-          if (!Tr::kSharedEmpty) tc::commit(&k_empty[s]);
-          if (jq == it.ntiles - 1) tc::commit(q_empty);  // Q no longer read
-        }
-        __syncwarp();
-      };
-      wait(q_full, (uint32_t)(a & 1), 50);
-      issue_qk(0);
-      for (int j = 0; j < it.ntiles; ++j) {
-        const int Tj = tctr + j;
-        if (j + 1 < it.ntiles) issue_qk(j + 1);
-        const int s = Tj % Tr::kStages;
-        {
-          const uint32_t pp = (uint32_t)((Tj >> 1) & 1), pv = (uint32_t)((Tj / Tr::kStages) & 1);
-          if (failed || !mbar_try_wait2(&p_full[Tj & 1], pp, &v_full[s], pv)) {
-            wait(&p_full[Tj & 1], pp, 300);
-            wait(&v_full[s], pv, 400);
-          }
-        }
-        if (j == 0 && a >= 1) wait(o_free, (uint32_t)((a - 1) & 1), 450);
-        // keys past the item's range: zero their V rows so P = 0 never meets a
-        // stale or non-finite value
-        const int valid = it.k1 - (it.k0 + j * kBN);
-        if (valid < kBN) {
-          uint8_t* vt = sV + s * Tr::kKVBytes;
-          const int nrow = kBN - valid;
-          for (int e = lane; e < nrow * Tr::kHalves * 8; e += 32) {
-            const int r = valid + e / (Tr::kHalves * 8);
-            const int rest = e % (Tr::kHalves * 8);
-            *reinterpret_cast<uint4*>(vt + (rest >> 3) * Tr::kSlab + r * 128 + (rest & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
           __syncwarp();
         }
-        tc::fence_after_sync();
-        if (lane == 0) {
-          const uint64_t dV = dV0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
-          const uint32_t tP = tS[Tj & 1];
+      } else {
+        for (int j = 0; j < it.ntiles; ++j) {
+          const int Tj = tctr + j;
+          const int s = Tj % Tr::kStages;
+          {
+            const uint32_t pp = (uint32_t)((Tj >> 1) & 1);
+            if (failed || !mbar_try_wait2(&p_full[Tj & 1], pp, &v_full[s], kv_par(Tj))) {
+              wait(&p_full[Tj & 1], pp, 300);
+              wait(&v_full[s], kv_par(Tj), 400);
+            }
+          }
+          if (j == 0 && a >= 1) wait(o_free, (uint32_t)((a - 1) & 1), 450);
+          // keys past the item's range: zero their V rows so P = 0 never meets a
+          // stale or non-finite value
+          const int valid = it.k1 - (it.k0 + j * kBN);
+          if (valid < kBN) {
+            uint8_t* vt = sV + s * Tr::kKVBytes;
+            const int nrow = kBN - valid;
+            for (int e = lane; e < nrow * Tr::kHalves * 8; e += 32) {
+              const int r = valid + e / (Tr::kHalves * 8);
+              const int rest = e % (Tr::kHalves * 8);
+              *reinterpret_cast<uint4*>(vt + (rest >> 3) * Tr::kSlab + r * 128 + (rest & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          tc::fence_after_sync();
+          if (lane == 0) {
+            const uint64_t dV = dV0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
+            const uint32_t tP = tS[Tj & 1];
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            tc::mma_f16_ts(tO, tP + kk * 8, dV + (kk * 2048 >> 4), id_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(&pv_done[Tj & 1]);
-          if (!Tr::kSharedEmpty) tc::commit(&v_empty[s]);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc::mma_f16_ts(tO, tP + kk * 8, dV + (kk * 2048 >> 4), id_pv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+            tc::commit(&pv_done[Tj & 1]);
+            if (!Tr::kSharedEmpty) tc::commit(&v_empty[s]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
       }
       tctr += it.ntiles;
       ++a;
     }
-    // every tcgen05 operation of this thread has completed once this arrives
+    // every tcgen05 operation of both issuers has completed once both arrive
     if (lane == 0) tc::commit(mma_fin);
     __syncwarp();
     wait(mma_fin, 0, 900);
@@ -728,8 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P (16-bit) goes into TMEM over this tile's S: the row's 64 keys of
         // this half -> columns [32 hf, 32 hf + 32) of the S buffer (both halves
         // of the row loaded their S before the exchange above).  P V of the
-        // tile two back, which read the previous P there, was issued before the
-        // Q K^T that wrote this S, so no wait is needed.
+        // tile two back, which read the previous P there, completed before the
+        // Q K^T that wrote this S was issued, so no wait is needed.
         if (quarter_live) {
           const float neg_m = -m_use;
           float rs8[8];
