@@ -24,9 +24,9 @@
 //              8 pages of K (warps 8-9) and of V (warps 10-11), each page
 //              resolved absolutely from the block table.
 //   warp 12    TMEM owner and P V issuer: O += P V with P read from TMEM.
-//   warp 13    Q K^T issuer: S into one of two TMEM buffers, tile t once P V of
-//              tile t-2 (whose P occupies the buffer) has completed.
-// TMEM: S0 (then P0) cols [0,128), S1 (then P1) [128,256), O [256, 256+D).
+//   warp 13    Q K^T issuer: S into one of three TMEM buffers, tile t once P V
+//              of tile t-3 (whose P occupies the buffer) has completed.
+// TMEM: S/P of tile t in cols [128 (t % 3), +128), O [384, 384+D).
 // Pipeline state (stage and buffer parities) runs on across items.
 #include <type_traits>
 
@@ -41,6 +41,12 @@ namespace {
 constexpr int kBM = 128;                 // tile rows
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kTilePages = kBN / kPage;  // 8
+// S/P buffers in TMEM (128 columns each; O follows them).  Q K^T of tile t
+// reuses the buffer of tile t-3 once P V of that tile has completed, so the
+// chain softmax(t) -> P V(t) -> Q K^T(t+3) -> softmax(t+3) spans three tiles.
+constexpr int kSBufs = 3;
+__device__ __forceinline__ int sbuf(int t) { return t % kSBufs; }
+__device__ __forceinline__ uint32_t sbuf_par(int t) { return (uint32_t)((t / kSBufs) & 1); }
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
 constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
@@ -61,7 +67,7 @@ struct EngTraits {
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffPre = kOffV + kStages * kKVBytes;  // two int[kEngineMaxB + 1] prefix sums
   static constexpr int kOffBar = kOffPre + ((2 * (kEngineMaxB + 1) * 4 + 15) & ~15);
-  static constexpr int kNumBars = 2 + 4 * kStages + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kNumBars = 2 + 4 * kStages + 3 * kSBufs + 1 + 1;
   // With two stages a K stage is free exactly when Q K^T of the tile two back
   // has completed, which s_full of that parity already signals; likewise a V
   // stage and pv_done.  The producers then wait on those, and the MMA thread
@@ -270,15 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = k_full + Tr::kStages;
   uint64_t* k_empty = v_full + Tr::kStages;
   uint64_t* v_empty = k_empty + Tr::kStages;
-  uint64_t* s_full = v_empty + Tr::kStages;  // [2]
-  // [2] by tile parity: with P in TMEM the softmax warps never wait for the
-  // previous P V, and they are synchronised only in pairs, so one lane quarter
-  // may arrive for tile j+1 before another has arrived for tile j.  It also
-  // tells the MMA thread that S of the tile is no longer read: Q K^T of tile
-  // j+2 is issued only after P V of tile j, which waited for p_full of j.
-  uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 2;  // [2]: P V of a tile of that parity completed
-  uint64_t* o_free = pv_done + 2;
+  uint64_t* s_full = v_empty + Tr::kStages;  // [kSBufs], tile t -> t % kSBufs
+  // [kSBufs] by S buffer: the softmax warps are synchronised only in pairs,
+  // so one lane quarter may arrive for tile t+1 or t+2 before another has
+  // arrived for tile t (t+3 needs P V of t); one barrier per buffer keeps
+  // those arrivals apart.
+  uint64_t* p_full = s_full + kSBufs;
+  uint64_t* pv_done = p_full + kSBufs;  // [kSBufs]: P V of a tile of that buffer completed
+  uint64_t* o_free = pv_done + kSBufs;
   uint64_t* mma_fin = o_free + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Tr::kOffMisc);
   int* misc = reinterpret_cast<int*>(smem + Tr::kOffMisc + 16);
@@ -294,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) mbar_init(&s_full[i], 1);
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&p_full[i], kSoftWarps);
       mbar_init(&pv_done[i], 1);
     }
@@ -392,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = *tslot;
-  const uint32_t tS[2] = {tbase, tbase + 128};
-  const uint32_t tO = tbase + 256;
+  const uint32_t tO = tbase + kSBufs * 128;
+  auto tS = [&](int t) { return tbase + (uint32_t)(sbuf(t) * 128); };
   const int total = sc.total0 + sc.total1;
 
   if (warp >= kWarpTMA && warp < kWarpMMA) {
@@ -416,7 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_v = pw >= kProdWarps / 2;
     const int sub = pw % (kProdWarps / 2);
     uint64_t* x_full = is_v ? v_full : k_full;
-    uint64_t* x_empty = Tr::kSharedEmpty ? (is_v ? pv_done : s_full) : (is_v ? v_empty : k_empty);
+    uint64_t* x_empty = is_v ? v_empty : k_empty;
+    // with two stages, stage of tile t is free once Q K^T (K) or P V (V) of
+    // tile t-2 has completed: s_full / pv_done of that tile
+    uint64_t* x_done = is_v ? pv_done : s_full;
     uint8_t* sX = is_v ? sV : sK;
     const CUtensorMap* tm_x = is_v ? &tm_v : &tm_k;
     bool failed = false;
@@ -492,7 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mc3 = c3[i];
           }
         if (lane == 0) {
-          if (!failed && !mbar_wait(&x_empty[s], par ^ 1)) {
+          const bool ok =
+              failed || (Tr::kSharedEmpty
+                             ? (Tj < 2 || mbar_wait(&x_done[sbuf(Tj - 2)], sbuf_par(Tj - 2)))
+                             : mbar_wait(&x_empty[s], par ^ 1));
+          if (!ok) {
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane 0 and each committing its own instructions.  Split in two, each
     // issuer's chain of barrier round trips and commits per tile is half as
     // long, and the two chains overlap.  Q K^T of tile t writes the TMEM
-    // buffer that holds P of tile t-2, so it waits for P V of that tile.
+    // buffer that holds P of tile t-3, so it waits for P V of that tile.
     bool failed = false;
     auto wait = [&](uint64_t* bar, uint32_t par, int where) {
       if (!failed && !mbar_wait(bar, par)) {
@@ -543,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < it.ntiles; ++j) {
           const int Tq = tctr + j;
           const int s = Tq % Tr::kStages;
-          if (Tq >= 2) {
-            const uint32_t pd = (uint32_t)(((Tq - 2) >> 1) & 1);
-            if (failed || !mbar_try_wait2(&k_full[s], kv_par(Tq), &pv_done[Tq & 1], pd)) {
+          if (Tq >= kSBufs) {
+            const uint32_t pd = sbuf_par(Tq - kSBufs);
+            if (failed || !mbar_try_wait2(&k_full[s], kv_par(Tq), &pv_done[sbuf(Tq)], pd)) {
               wait(&k_full[s], kv_par(Tq), 100);
-              wait(&pv_done[Tq & 1], pd, 200);
+              wait(&pv_done[sbuf(Tq)], pd, 200);
             }
           } else {
             wait(&k_full[s], kv_par(Tq), 100);
@@ -555,13 +567,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_after_sync();
           if (lane == 0) {
             const uint64_t dK = dK0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
-            const uint32_t tSq = tS[Tq & 1];
+            const uint32_t tSq = tS(Tq);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = ((kk >> 2) * Tr::kSlab + (kk & 3) * 32) >> 4;
               tc::mma_f16_ss(tSq, dQ + off, dK + off, id_qk, kk > 0);
             }
-            tc::commit(&s_full[Tq & 1]);
+            tc::commit(&s_full[sbuf(Tq)]);
             if (!Tr::kSharedEmpty) tc::commit(&k_empty[s]);
             if (j == it.ntiles - 1) tc::commit(q_empty);  // Q no longer read
           }
@@ -572,9 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int Tj = tctr + j;
           const int s = Tj % Tr::kStages;
           {
-            const uint32_t pp = (uint32_t)((Tj >> 1) & 1);
-            if (failed || !mbar_try_wait2(&p_full[Tj & 1], pp, &v_full[s], kv_par(Tj))) {
-              wait(&p_full[Tj & 1], pp, 300);
+            const uint32_t pp = sbuf_par(Tj);
+            if (failed || !mbar_try_wait2(&p_full[sbuf(Tj)], pp, &v_full[s], kv_par(Tj))) {
+              wait(&p_full[sbuf(Tj)], pp, 300);
               wait(&v_full[s], kv_par(Tj), 400);
             }
           }
@@ -597,12 +609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_after_sync();
           if (lane == 0) {
             const uint64_t dV = dV0 + (uint32_t)((s * Tr::kKVBytes) >> 4);
-            const uint32_t tP = tS[Tj & 1];
+            const uint32_t tP = tS(Tj);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
               tc::mma_f16_ts(tO, tP + kk * 8, dV + (kk * 2048 >> 4), id_pv,
                              (j > 0 || kk > 0) ? 1u : 0u);
-            tc::commit(&pv_done[Tj & 1]);
+            tc::commit(&pv_done[sbuf(Tj)]);
             if (!Tr::kSharedEmpty) tc::commit(&v_empty[s]);
           }
           __syncwarp();
@@ -699,8 +711,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_use = neg_inf(), l = 0.f;
       for (int j = 0; j < it.ntiles; ++j) {
         const int Tj = tctr + j;
-        const uint32_t tSj = tS[Tj & 1] + lane_off + hf * 64;
-        wait(&s_full[Tj & 1], (uint32_t)((Tj >> 1) & 1), 500);
+        const uint32_t tSj = tS(Tj) + lane_off + hf * 64;
+        wait(&s_full[sbuf(Tj)], sbuf_par(Tj), 500);
         tc::fence_after_sync();
         // keys [0, lim) of this half's 64 columns are visible to the row
         const int lim = vis_end - (it.k0 + j * kBN + hf * 64);
@@ -745,8 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P (16-bit) goes into TMEM over this tile's S: the row's 64 keys of
         // this half -> columns [32 hf, 32 hf + 32) of the S buffer (both halves
         // of the row loaded their S before the exchange above).  P V of the
-        // tile two back, which read the previous P there, completed before the
-        // Q K^T that wrote this S was issued, so no wait is needed.
+        // tile three back, which read the previous P there, completed before
+        // the Q K^T that wrote this S was issued, so no wait is needed.
         if (quarter_live) {
           const float neg_m = -m_use;
           float rs8[8];
@@ -767,13 +779,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               rs8[i & 7] += e0 + e1;
               pk[i] = E::from_f2(e0, e1);
             }
-            tc::tmem_st16u(tS[Tj & 1] + lane_off + hf * 32 + q2 * 16, pk);
+            tc::tmem_st16u(tS(Tj) + lane_off + hf * 32 + q2 * 16, pk);
           }
           l += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         }
         if (j >= 1 && quarter_live && __any_sync(0xffffffffu, rescale)) {
           // O is stable once P V of the previous tile is done
-          wait(&pv_done[(Tj - 1) & 1], (uint32_t)(((Tj - 1) >> 1) & 1), 650);
+          wait(&pv_done[sbuf(Tj - 1)], sbuf_par(Tj - 1), 650);
           tc::fence_after_sync();
           const float sa = rescale ? alpha : 1.f;
 #pragma unroll 1
@@ -791,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&p_full[Tj & 1]);
+          mbar_arrive(&p_full[sbuf(Tj)]);
         }
       }
       // ---- epilogue: the two halves' sums, then O / l and LSE
@@ -802,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float L = xl[r];
       {
         const int tl = tctr + it.ntiles - 1;
-        wait(&pv_done[tl & 1], (uint32_t)((tl >> 1) & 1), 700);
+        wait(&pv_done[sbuf(tl)], sbuf_par(tl), 700);
       }
       tc::fence_after_sync();
       const float inv = L > 0.f ? 1.f / L : 0.f;
