@@ -23,8 +23,10 @@
 //   warps 8-11 TMA producers: Q of the item (warp 8), then per 128-key tile
 //              8 pages of K (warps 8-9) and of V (warps 10-11), each page
 //              resolved absolutely from the block table.
-//   warp 12    TMEM owner and P V issuer: O += P V with P read from TMEM.
-//   warp 13    Q K^T issuer: S into one of three TMEM buffers, tile t once P V
+//   warps 12-13 idle: they only place the issuers below on the schedulers
+//              (warp % 4) of the V producers, away from the K producers'.
+//   warp 14    TMEM owner and P V issuer: O += P V with P read from TMEM.
+//   warp 15    Q K^T issuer: S into one of three TMEM buffers, tile t once P V
 //              of tile t-3 (whose P occupies the buffer) has completed.
 // TMEM: S/P of tile t in cols [128 (t % 3), +128), O [384, 384+D).
 // Pipeline state (stage and buffer parities) runs on across items.
@@ -51,9 +53,12 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
 constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
 constexpr int kWarpTMA = kSoftWarps;        // first TMA producer warp
-constexpr int kWarpMMA = kSoftWarps + kProdWarps;  // P V issuer + TMEM owner
+// Warps 12 and 13 do nothing: with 16 warps the two MMA issuers land on the
+// schedulers of warps 2/6/10 and 3/7/11 (measured: +5 % prefill throughput
+// over issuers on the schedulers shared with warps 0/4/8 and 1/5/9).
+constexpr int kWarpMMA = kSoftWarps + kProdWarps + 2;  // P V issuer + TMEM owner
 constexpr int kWarpQK = kWarpMMA + 1;               // Q K^T issuer
-constexpr int kThreads = (kSoftWarps + kProdWarps + 2) * 32;
+constexpr int kThreads = (kSoftWarps + kProdWarps + 4) * 32;
 
 template <int D>
 struct EngTraits {
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tS = [&](int t) { return tbase + (uint32_t)(sbuf(t) * 128); };
   const int total = sc.total0 + sc.total1;
 
-  if (warp >= kWarpTMA && warp < kWarpMMA) {
+  if (warp >= kWarpTMA && warp < kWarpTMA + kProdWarps) {
     // ======================= TMA producers =======================
     // Warps 0 and 1 of the group load K tiles, warps 2 and 3 V tiles, each
     // taking alternate pages of every tile (TMA issue throughput grows with
@@ -521,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMMA || warp == kWarpQK) {
     // ======================= MMA issuers =======================
-    // Warp 13 issues every S = Q K^T, warp 12 every O += P V, each from its
+    // Warp 15 issues every S = Q K^T, warp 14 every O += P V, each from its
     // lane 0 and each committing its own instructions.  Split in two, each
     // issuer's chain of barrier round trips and commits per tile is half as
     // long, and the two chains overlap.  Q K^T of tile t writes the TMEM
@@ -627,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) tc::commit(mma_fin);
     __syncwarp();
     wait(mma_fin, 0, 900);
-  } else {
+  } else if (warp < kSoftWarps) {
     // ======================= softmax warps 0-7 =======================
     // Warps w and w+4 own tile rows 32*(w%4) .. +31 (the TMEM lane quarter a
     // warp may access); warp w < 4 takes S columns 0-63 and O columns
