@@ -125,7 +125,8 @@ def mma_rate(dev):
     """Back-to-back kind::f16 MMAs of M=128, K=16 on every SM (one CTA each):
     cycles per instruction on the SM clock and the whole-GPU rate from CUDA
     events, for the engine's shapes (N=128 keys for Q K^T, N=D=128 with P in
-    TMEM for P V) and for N=256."""
+    TMEM for P V) and for N=256, with the issuing thread's descriptors built
+    once (lean) or per instruction."""
     import ctypes
 
     import torch
@@ -139,13 +140,13 @@ def mma_rate(dev):
     grid = torch.cuda.get_device_properties(dev).multi_processor_count
     tpeak, tsrc = read_tensor_peak()
     n = 4096
-    for N, ts, ks in ((128, 0, 4), (128, 0, 8), (128, 1, 4), (128, 1, 8), (256, 0, 4), (256, 0, 8)):
+    for N, ts, lean in ((128, 0, 1), (128, 1, 1), (256, 0, 1), (128, 0, 0), (128, 1, 0), (256, 0, 0)):
         cyc = (ctypes.c_longlong * 2)()
         ms = ctypes.c_float()
-        rc = lib.pa_selftest_mma_rate(n, N, ts, ks, grid, cyc, ctypes.byref(ms))
+        rc = lib.pa_selftest_mma_rate(n, N, ts, lean, grid, cyc, ctypes.byref(ms))
         tf = 2.0 * 128 * N * 16 * n * grid / (ms.value * 1e-3) / 1e12 if rc == 0 else None
         print(json.dumps({"mma_rate": f"M=128 N={N} K=16 kind::f16, A from {'TMEM' if ts else 'SMEM'}",
-                          "ksteps": ks,
+                          "issue": "descriptors built once" if lean else "descriptors per instruction",
                           "rc": rc, "instr_per_cta": n, "ctas": grid,
                           "cycles_per_instr": round(cyc[1] / n, 1) if rc == 0 else None,
                           "tflops": round(tf, 1) if tf else None,

@@ -2,12 +2,16 @@
 // (one per SM) issues `n_instr` back-to-back kind::f16 MMAs of M = 128,
 // K = 16 and N in {128, 256} into one TMEM accumulator, A from shared memory
 // or from TMEM, and its first thread times issue and completion with the SM
-// clock.  `ksteps` = 4 cycles through the four 16-element k-steps of one
-// 128-byte slab (operands repeat every 4 instructions); 8 walks two slabs, so
-// every instruction of a K = 128 product reads distinct operand bytes, as the
-// attention tiles do.  Attention with head dim 128 runs Q K^T at N = 128 keys per tile and
-// P V at N = D = 128; this measures what that shape can reach on the hardware,
-// next to the N = 256 shape a plain GEMM uses.
+// clock.  Every group of 8 instructions walks the 8 k-steps of a K = 128
+// product over two 128-byte-swizzled slabs, so each instruction reads distinct
+// operand bytes, as the attention tiles do.
+//   lean = 1: descriptors built once, k-steps unrolled with constant offsets
+//             (the issuing thread spends a few instructions per MMA);
+//   lean = 0: descriptors rebuilt per instruction in a runtime loop.
+// The two show how much of an MMA stream's rate the single issuing thread's
+// own instructions can cost: at N = 128 the tensor pipe takes about 64 SM
+// cycles per instruction, close to what a thread spends building two
+// descriptors and the loop around them.
 #include <cuda_runtime.h>
 
 #include "pa_common.cuh"
@@ -18,8 +22,9 @@ namespace {
 
 constexpr int kRateSmem = 120 * 1024;  // one CTA per SM
 
-__global__ void __launch_bounds__(128, 1)
-    mma_rate_kernel(int n_instr, int N, int a_in_tmem, int ksteps, long long* cycles) {
+template <int N, bool kTS, bool kLean>
+__global__ void __launch_bounds__(128, 1) mma_rate_kernel(int n_instr, long long* cycles) {
+  constexpr bool a_in_tmem = kTS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -61,15 +66,32 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t id = tc::idesc_f16(128, N, false, false);
     const uint32_t aA = smem_u32(sA), aB = smem_u32(sB);
     const long long t0 = clock64();
-    for (int i = 0; i < n_instr; ++i) {
-      const int kk = ksteps == 8 ? (i & 7) : (i & 3);
-      const uint32_t offA = (kk >> 2) * 16384 + (kk & 3) * 32;
-      const uint32_t offB = (kk >> 2) * (N * 128) + (kk & 3) * 32;
-      if (a_in_tmem)
-        tc::mma_f16_ts(tbase, tbase + 384 + kk * 8, tc::smem_desc(aB + offB, 16, 1024), id, 1);
-      else
-        tc::mma_f16_ss(tbase, tc::smem_desc(aA + offA, 16, 1024),
-                       tc::smem_desc(aB + offB, 16, 1024), id, 1);
+    if (kLean) {
+      const uint64_t dA = tc::smem_desc(aA, 16, 1024);
+      const uint64_t dB = tc::smem_desc(aB, 16, 1024);
+      constexpr uint32_t slabB = (uint32_t)(N * 128) >> 4;  // second slab of B, descriptor units
+      for (int o = 0; o < n_instr / 8; ++o) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t offA = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          const uint32_t offB = (kk >> 2) * slabB + (((kk & 3) * 32) >> 4);
+          if (a_in_tmem)
+            tc::mma_f16_ts(tbase, tbase + 384 + kk * 8, dB + offB, id, 1);
+          else
+            tc::mma_f16_ss(tbase, dA + offA, dB + offB, id, 1);
+        }
+      }
+    } else {
+      for (int i = 0; i < n_instr / 8 * 8; ++i) {
+        const int kk = i & 7;
+        const uint32_t offA = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t offB = (kk >> 2) * (N * 128) + (kk & 3) * 32;
+        if (a_in_tmem)
+          tc::mma_f16_ts(tbase, tbase + 384 + kk * 8, tc::smem_desc(aB + offB, 16, 1024), id, 1);
+        else
+          tc::mma_f16_ss(tbase, tc::smem_desc(aA + offA, 16, 1024),
+                         tc::smem_desc(aB + offB, 16, 1024), id, 1);
+      }
     }
     const long long t1 = clock64();
     tc::commit(bar);
@@ -86,38 +108,53 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tc::tmem_dealloc(tbase, 512);
 }
 
-}  // namespace
-}  // namespace pa
-
-// n_instr MMAs per CTA on `grid` CTAs (one per SM); N = 128 or 256 (256 only
-// with A in shared memory); ksteps = 4 or 8 (see above).  Fills cycles[0] = issue, cycles[1] = completion
-// (SM clocks of CTA 0; -1 if the completion wait timed out) and *ms = the
-// CUDA-event time of the timed launch (after one untimed launch).  Returns 0,
-// or a negative code for invalid arguments / CUDA errors.
-extern "C" __attribute__((visibility("default"))) int pa_selftest_mma_rate(
-    int n_instr, int N, int a_in_tmem, int ksteps, int grid, long long* cycles, float* ms) {
-  if (n_instr < 1 || grid < 1 || (N != 128 && N != 256) || (a_in_tmem && N != 128) ||
-      (ksteps != 4 && ksteps != 8))
-    return -1;
-  if (cudaFuncSetAttribute(pa::mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           pa::kRateSmem) != cudaSuccess)
+template <int N, bool kTS, bool kLean>
+int run(int n_instr, int grid, long long* d, float* ms) {
+  if (cudaFuncSetAttribute(mma_rate_kernel<N, kTS, kLean>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem) != cudaSuccess)
     return -2;
-  long long* d = nullptr;
-  if (cudaMalloc(&d, 2 * sizeof(long long)) != cudaSuccess) return -3;
   cudaEvent_t e0, e1;
   cudaEventCreate(&e0);
   cudaEventCreate(&e1);
-  pa::mma_rate_kernel<<<grid, 128, pa::kRateSmem>>>(n_instr, N, a_in_tmem, ksteps, d);
+  mma_rate_kernel<N, kTS, kLean><<<grid, 128, kRateSmem>>>(n_instr, d);
   cudaEventRecord(e0);
-  pa::mma_rate_kernel<<<grid, 128, pa::kRateSmem>>>(n_instr, N, a_in_tmem, ksteps, d);
+  mma_rate_kernel<N, kTS, kLean><<<grid, 128, kRateSmem>>>(n_instr, d);
   cudaEventRecord(e1);
   int rc = cudaEventSynchronize(e1) == cudaSuccess ? 0 : -4;
-  if (rc == 0) {
-    cudaEventElapsedTime(ms, e0, e1);
-    if (cudaMemcpy(cycles, d, 2 * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) rc = -5;
-  }
+  if (rc == 0) cudaEventElapsedTime(ms, e0, e1);
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  return rc;
+}
+
+}  // namespace
+}  // namespace pa
+
+// n_instr (a multiple of 8) MMAs per CTA on `grid` CTAs (one per SM); N = 128
+// or 256 (256 only with A in shared memory); lean = 1 or 0 (see above).
+// Fills cycles[0] = issue, cycles[1] = completion (SM clocks of CTA 0; -1 if
+// the completion wait timed out) and *ms = the CUDA-event time of the timed
+// launch (after one untimed launch).  Returns 0, or a negative code for
+// invalid arguments / CUDA errors.
+extern "C" __attribute__((visibility("default"))) int pa_selftest_mma_rate(
+    int n_instr, int N, int a_in_tmem, int lean, int grid, long long* cycles, float* ms) {
+  if (n_instr < 8 || n_instr % 8 != 0 || grid < 1 || (N != 128 && N != 256) ||
+      (a_in_tmem && N != 128) || (lean != 0 && lean != 1))
+    return -1;
+  long long* d = nullptr;
+  if (cudaMalloc(&d, 2 * sizeof(long long)) != cudaSuccess) return -3;
+  int rc;
+  if (N == 256)
+    rc = lean ? pa::run<256, false, true>(n_instr, grid, d, ms)
+              : pa::run<256, false, false>(n_instr, grid, d, ms);
+  else if (a_in_tmem)
+    rc = lean ? pa::run<128, true, true>(n_instr, grid, d, ms)
+              : pa::run<128, true, false>(n_instr, grid, d, ms);
+  else
+    rc = lean ? pa::run<128, false, true>(n_instr, grid, d, ms)
+              : pa::run<128, false, false>(n_instr, grid, d, ms);
+  if (rc == 0 && cudaMemcpy(cycles, d, 2 * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess)
+    rc = -5;
   cudaFree(d);
   return rc;
 }
