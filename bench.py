@@ -247,7 +247,7 @@ def secondary_measurements(dev, only=None):
             "us": round(us, 1), "tflops": round(fl / us / 1e6, 1),
             "roofline": {"bound": "tensor", "achieved": round(fl / us / 1e6, 1), "peak": tpeak,
                          "unit": "TFLOP/s", "frac": round(fl / us / 1e6 / tpeak, 4),
-                         "peak_source": tsrc, "kernel": "prefill_kernel<128, half>"},
+                         "peak_source": tsrc, "kernel": "engine_kernel<128, __half>"},
             "flops": fl, "us_with_append": round(us_append, 1),
             "note": "fp16, 32 heads x D 128, causal, keys read through 16-token pages"}
         if only == "prefill":
@@ -312,6 +312,19 @@ def secondary_measurements(dev, only=None):
                                    "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4),
                                    "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4)}
     del w, out, ws
+    # multi-query (speculative) decode: 6 new tokens per sequence appended in the
+    # call, causal among themselves, 64 sequences x ctx 4096, GQA 32/8, D 128, bf16
+    w = wl.paged_decode(batch=64, ctx=4096, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        dtype="bf16", lnew=6, seed=1010, device=dev)
+    out = torch.empty_like(w["q"])
+    fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                   w["block_table"], k=w["k_new"], v=w["v_new"], causal=True,
+                                   out=out, return_lse=False)
+    us = time_calls(fn, 50, 5, stream)
+    by = algorithmic_bytes(64, 4096, 6, 6, 32, 8, 128)
+    res["spec_decode_lq6_b64_ctx4096"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
+                                          "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4)}
+    del w, out
     # tiny paged decode (launch-latency bound)
     w = wl.tiny_decode(device=dev)
     fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
