@@ -84,11 +84,15 @@ def attention_flops(q_lens, k_lens, heads, d, causal):
     return 4 * d * heads * total
 
 
-def time_calls(fn, steps, warmup, stream, graph=True):
+def time_calls(fn, steps, warmup, stream, graph=True, flush=False):
     """Device time per call in us.  With `graph`, `steps` calls are captured in
     one CUDA graph and replayed, so host launch overhead does not show up as
     idle device time for short kernels (the library never synchronises or
-    reads lengths on the host, so its calls capture as they are)."""
+    reads lengths on the host, so its calls capture as they are).  With
+    `flush`, every call is preceded by a 256 MB write (twice the L2) outside
+    its own event pair: for workloads whose inputs would otherwise stay in L2
+    between calls; the call's launches are queued behind the flush, so no host
+    gap shows up inside the pair."""
     import torch
 
     for _ in range(warmup):
@@ -96,6 +100,17 @@ def time_calls(fn, steps, warmup, stream, graph=True):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if flush:
+        scratch = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)]
+        for a, b in pairs:
+            scratch.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in pairs) / steps * 1e3
     if graph:
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
@@ -252,19 +267,19 @@ def secondary_measurements(dev, only=None):
             "note": "fp16, 32 heads x D 128, causal, keys read through 16-token pages"}
         if only == "prefill":
             return res
-    # the small-page reproduction shapes: 4 x 170 new tokens over a cached prefix
-    w = wl.prefill_append(device=dev, seed=1004)
-    out = torch.empty_like(w["q"])
-    fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
-                                   w["block_table"], k=w["k_new"], v=w["v_new"], causal=True,
-                                   out=out, return_lse=False)
-    us = time_calls(fn, 50, 5, stream)
-    old = w["cache_seqlens"].cpu().tolist()
-    fl = attention_flops([170] * 4, [o + 170 for o in old], 32, 128, True)
-    res["prefill_append_4x170"] = {"us": round(us, 1), "tflops": round(fl / us / 1e6, 2),
-                                   "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4)}
-    if only not in (None, "gqa"):
-        return res
+    if only is None:
+        # the small-page reproduction shapes: 4 x 170 new tokens over a cached prefix
+        w = wl.prefill_append(device=dev, seed=1004)
+        out = torch.empty_like(w["q"])
+        fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                       w["block_table"], k=w["k_new"], v=w["v_new"], causal=True,
+                                       out=out, return_lse=False)
+        us = time_calls(fn, 50, 5, stream, flush=True)
+        old = w["cache_seqlens"].cpu().tolist()
+        fl = attention_flops([170] * 4, [o + 170 for o in old], 32, 128, True)
+        res["prefill_append_4x170"] = {"us": round(us, 1), "tflops": round(fl / us / 1e6, 2),
+                                       "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4),
+                                       "l2": "flushed between calls"}
     # GQA split-KV decode on a contiguous 131072-token cache, lengths U[1024, 8192]
     w = wl.gqa_contiguous(device=dev)
     kc = torch.empty((8, w["capacity"], 8, 128), dtype=torch.bfloat16, device=dev)
@@ -279,13 +294,16 @@ def secondary_measurements(dev, only=None):
                      dtype=torch.uint8, device=dev)
     fn = lambda: pa.pa_fwd_kvcache(w["q"], kc, vc, w["cache_seqlens"], None, out=out, lse=lse,  # noqa: E731
                                    workspace=ws)
-    us = time_calls(fn, 100 if only is None else 3, 10 if only is None else 3, stream,
-                    graph=only is None)
+    # 132 MB of K/V against a 129 MB L2 (loaded evict-last): flush between calls
+    us = time_calls(fn, 50 if only is None else 3, 10 if only is None else 3, stream, flush=True)
+    us_warm = time_calls(fn, 100, 10, stream) if only is None else None
     lens = w["cache_seqlens"].cpu().tolist()
     by = sum(lens) * 8 * 128 * 2 * 2 + 8 * 32 * 128 * 2 * 2
     res["gqa_contiguous_split_kv"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
                                       "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4),
-                                      "mean_len": sum(lens) / len(lens)}
+                                      "mean_len": sum(lens) / len(lens),
+                                      "l2": "flushed between calls",
+                                      "us_l2_warm": None if us_warm is None else round(us_warm, 1)}
     del kc, vc
     if only == "gqa":
         return res
