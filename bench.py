@@ -343,6 +343,23 @@ def secondary_measurements(dev, only=None):
     res["spec_decode_lq6_b64_ctx4096"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
                                           "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4)}
     del w, out
+    # rotary embedding of the new token (its own kernel ahead of the decode):
+    # the same paged decode step with and without it, B64 x ctx 4096, 32x128, fp16
+    w = wl.paged_decode(batch=64, ctx=4096, lnew=1, seed=1011, device=dev)
+    out = torch.empty_like(w["q"])
+    ang = torch.arange(4096, dtype=torch.float64, device=dev)[:, None] * (
+        10000.0 ** (-2.0 * torch.arange(64, dtype=torch.float64, device=dev) / 128))[None, :]
+    cos, sin = ang.cos().half(), ang.sin().half()
+    plain = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                      w["block_table"], k=w["k_new"], v=w["v_new"], out=out,
+                                      return_lse=False)
+    rotary = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                       w["block_table"], k=w["k_new"], v=w["v_new"], out=out,
+                                       return_lse=False, rotary_cos=cos, rotary_sin=sin)
+    us_plain = time_calls(plain, 50, 5, stream)
+    us_rot = time_calls(rotary, 50, 5, stream)
+    res["rotary_decode_b64_ctx4096"] = {"us": round(us_rot, 1), "us_without_rotary": round(us_plain, 1)}
+    del w, out
     # tiny paged decode (launch-latency bound)
     w = wl.tiny_decode(device=dev)
     fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731

@@ -159,6 +159,51 @@ PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int 
                                             int max_seqlen_k, int num_splits);
 
 /*
+ * pa_fwd_kvcache_rotary -- pa_fwd_kvcache with rotary position embedding of
+ * the new tokens.  flash-attention #824 "Add support for small page sizes"
+ * names the feature (a fix to fused RoPE embeddings in this forward) without
+ * defining it; the rotation is the published RoFormer one:
+ *
+ *   - features [0, rotary_dim) are rotated, the rest pass through;
+ *   - rotary_interleaved == 0: feature p pairs with p + rotary_dim / 2;
+ *     otherwise feature 2p pairs with 2p + 1;
+ *   - a pair (x1, x2) of a token at position pos becomes
+ *     (x1 c - x2 s, x1 s + x2 c), c = rotary_cos[pos][p], s = rotary_sin[pos][p].
+ *
+ * Positions: new token i of sequence b is at cache_seqlens[b] + i (the slot the
+ * append writes it to); query row i of Lq is at cache_seqlens[b] + Lnew - Lq + i.
+ * The rotated k is what the append stores in the cache; the rotated q is what
+ * attends.  The rotation is computed in fp32 and rounded once to the dtype.
+ *
+ * Arguments are those of pa_fwd_kvcache plus
+ *   rotary_cos, rotary_sin  [rotary_len, rotary_dim / 2], row-major, dtype of q;
+ *                           device memory owned by the caller.
+ *   rotary_len              rows of the tables; a position >= rotary_len
+ *                           leaves the token unrotated and records
+ *                           PA_DEVERR_LENGTH (sequence, position) in err_word.
+ *   rotary_dim              even, 2 <= rotary_dim <= D.
+ * Requires Lnew >= 1 (the rotation applies to appended tokens).  workspace:
+ * pa_fwd_kvcache_rotary_workspace_size bytes, 256-byte aligned (the rotated q
+ * and k_new live there for the call, ahead of pa_fwd_kvcache's own scratch).
+ * Runs one extra kernel (the rotation) ahead of the pa_fwd_kvcache launches on
+ * `stream`; same return codes as pa_fwd_kvcache.
+ */
+PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                                 pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                                 const void* v_new, int Lnew, const int32_t* cache_seqlens,
+                                 const int32_t* block_table, int64_t bt_stride, int max_pages,
+                                 int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
+                                 int max_seqlen_k, const void* rotary_cos, const void* rotary_sin,
+                                 int rotary_len, int rotary_dim, int rotary_interleaved,
+                                 float scale, int causal, int num_splits, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                 int dtype, pa_stream_t stream);
+
+/* Bytes of workspace pa_fwd_kvcache_rotary needs for these sizes. */
+PA_API size_t pa_fwd_kvcache_rotary_workspace_size(int B, int Lq, int Hq, int Hkv, int D, int Lnew,
+                                                   int max_seqlen_k, int num_splits);
+
+/*
  * pa_fwd_kvcache_noalloc -- pa_fwd_kvcache for callers that cannot allocate
  * device memory.  (No counterpart on the pages: this is a library-usage entry
  * point, not part of the attention method.)

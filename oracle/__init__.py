@@ -18,6 +18,8 @@ Sources (web pages this method is described on):
        cache whose real length comes from ``cache_seqlens``.
   [p4] vLLM #3010 "Introduce flash-attn (>= 2.5.0)" -- paged decode and
        prefill + cache-write benchmarks.
+Rotary embedding of the new tokens (``rotary.py``) is only named on [p1]; it
+follows the published RoFormer definition, see that module.
 
 Parity pins live in ``tests/test_oracle_pins.py``.  Every function here is
 pinned (golden worked examples under ``tests/golden/``, closed forms,
@@ -38,3 +40,4 @@ from .attention import (  # noqa: F401
     split_then_combine,
     combine_splits,
 )
+from .rotary import round_to, rotary, rotate_new_tokens  # noqa: F401

@@ -58,6 +58,12 @@ _SIGNATURES = {
                               _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
                               _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
     "pa_fwd_kvcache_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_fwd_kvcache_rotary": (_i32, [_vp, _i64, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp,
+                                     _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32,
+                                     _i64, _i32, _vp, _vp, _i32, _i32, _i32, _f32, _i32, _i32,
+                                     _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
+    "pa_fwd_kvcache_rotary_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                                   _i32]),
     "pa_fwd_kvcache_noalloc": (_i32, [_vp, _i64, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp,
                                       _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32,
                                       _i64, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _i32, _vp]),
@@ -148,13 +154,16 @@ def fwd_kvcache_workspace_size(B, Lq, Hq, Hkv, D, max_seqlen_k, num_splits=0):
 
 def pa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, k=None, v=None,
                    scale=None, causal=False, num_splits=0, out=None, lse=None, workspace=None,
-                   err=None, max_seqlen_k=None, return_lse=True):
+                   err=None, max_seqlen_k=None, return_lse=True, rotary_cos=None,
+                   rotary_sin=None, rotary_interleaved=False):
     """flash_attn_with_kvcache-style forward; returns ``(out, lse)``.
 
     q ``[B, Lq, Hq, D]``; caches paged ``[num_pages, 16, Hkv, D]`` with
     ``block_table [B, max_pages]`` (int32) or contiguous ``[B, capacity, Hkv, D]``;
     ``k``/``v`` ``[B, Lnew, Hkv, D]`` are appended in the same call.
     ``max_seqlen_k`` defaults to the capacity implied by the table/cache shape.
+    ``rotary_cos``/``rotary_sin`` ``[rotary_len, rotary_dim / 2]`` (q's dtype):
+    rotary embedding of the new tokens' q and k (pa_fwd_kvcache_rotary).
     """
     lib = load_library()
     _cuda(q, k_cache, v_cache, cache_seqlens, block_table, k, v)
@@ -178,6 +187,23 @@ def pa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, k=None,
         out = torch.empty((B, lq, hq, d), dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, hq, lq), dtype=torch.float32, device=q.device)
+    if rotary_cos is not None:
+        _cuda(rotary_cos, rotary_sin)
+        rotary_cos = rotary_cos.contiguous()
+        rotary_sin = rotary_sin.contiguous()
+        ws_bytes = lib.pa_fwd_kvcache_rotary_workspace_size(B, lq, hq, hkv, d, lnew, max_seqlen_k,
+                                                            num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+        ws_len = workspace.numel() * workspace.element_size()
+        _check(lib.pa_fwd_kvcache_rotary(
+            _ptr(q), q.stride(0), q.stride(1), q.stride(2), _t4(k_cache), _t4(v_cache), _ptr(k),
+            _ptr(v), lnew, _ptr(cache_seqlens), _ptr(block_table), bt_stride, max_pages, B, lq,
+            hq, hkv, d, extent, max_seqlen_k, _ptr(rotary_cos), _ptr(rotary_sin),
+            rotary_cos.shape[0], 2 * rotary_cos.shape[1], int(bool(rotary_interleaved)),
+            float(scale), int(bool(causal)), int(num_splits), _ptr(out), _ptr(lse),
+            _ptr(workspace), ws_len, _ptr(err), _dtype(q), _stream(q)))
+        return out, lse
     ws_bytes = lib.pa_fwd_kvcache_workspace_size(B, lq, hq, hkv, d, max_seqlen_k, num_splits)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)

@@ -261,6 +261,74 @@ PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int 
   return split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max).total;
 }
 
+// scratch for the rotated q and k_new, ahead of pa_fwd_kvcache's own workspace
+static size_t rotary_scratch_bytes(int B, int Lq, int Hq, int Hkv, int D, int Lnew) {
+  const size_t qb = ((size_t)B * Lq * Hq * D * 2 + 255) & ~(size_t)255;
+  const size_t kb = ((size_t)B * Lnew * Hkv * D * 2 + 255) & ~(size_t)255;
+  return qb + kb;
+}
+
+PA_API size_t pa_fwd_kvcache_rotary_workspace_size(int B, int Lq, int Hq, int Hkv, int D, int Lnew,
+                                                   int max_seqlen_k, int num_splits) {
+  if (B <= 0 || Lq <= 0 || Lnew <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+  return rotary_scratch_bytes(B, Lq, Hq, Hkv, D, Lnew) +
+         pa_fwd_kvcache_workspace_size(B, Lq, Hq, Hkv, D, max_seqlen_k, num_splits);
+}
+
+PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                                 pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                                 const void* v_new, int Lnew, const int32_t* cache_seqlens,
+                                 const int32_t* block_table, int64_t bt_stride, int max_pages,
+                                 int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
+                                 int max_seqlen_k, const void* rotary_cos, const void* rotary_sin,
+                                 int rotary_len, int rotary_dim, int rotary_interleaved,
+                                 float scale, int causal, int num_splits, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                 int dtype, pa_stream_t stream) {
+  int rc = check_common(dtype, D, Hq, Hkv);
+  if (rc) return rc;
+  if (B < 0 || Lq < 0) return fail(PA_ERR_INVALID_ARG, "negative B or Lq");
+  if (B == 0 || Lq == 0) return PA_OK;
+  if (Lnew < 1 || k_new == nullptr || v_new == nullptr || cache_seqlens == nullptr)
+    return fail(PA_ERR_INVALID_ARG,
+                "rotary embedding applies to appended tokens: needs Lnew >= 1, k_new, v_new and "
+                "cache_seqlens");
+  if (q == nullptr || rotary_cos == nullptr || rotary_sin == nullptr)
+    return fail(PA_ERR_INVALID_ARG, "q, rotary_cos and rotary_sin must be non-NULL");
+  if (rotary_dim < 2 || rotary_dim > D || rotary_dim % 2 != 0 || rotary_len < 1)
+    return fail(PA_ERR_INVALID_ARG, "rotary_dim must be even in [2, D] and rotary_len >= 1");
+  const size_t scratch = rotary_scratch_bytes(B, Lq, Hq, Hkv, D, Lnew);
+  if (workspace == nullptr || workspace_bytes < scratch ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(PA_ERR_WORKSPACE,
+                "workspace must be 256-byte aligned and hold "
+                "pa_fwd_kvcache_rotary_workspace_size bytes");
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  const size_t qb = ((size_t)B * Lq * Hq * D * 2 + 255) & ~(size_t)255;
+  RotaryParams rp{};
+  rp.q = q;
+  rp.q_sb = q_sb; rp.q_st = q_st; rp.q_sh = q_sh;
+  rp.k_new = k_new;
+  rp.q_out = ws;
+  rp.k_out = ws + qb;
+  rp.cos = rotary_cos;
+  rp.sin = rotary_sin;
+  rp.cache_seqlens = cache_seqlens;
+  rp.B = B; rp.Lq = Lq; rp.Lnew = Lnew; rp.Hq = Hq; rp.Hkv = Hkv; rp.D = D;
+  rp.rotary_dim = rotary_dim;
+  rp.rotary_len = rotary_len;
+  rp.interleaved = rotary_interleaved ? 1 : 0;
+  rp.err = err_word;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_rotary(rp, dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
+  const size_t rest = workspace_bytes - scratch;
+  return pa_fwd_kvcache(ws, (int64_t)Lq * Hq * D, (int64_t)Hq * D, D, k_cache, v_cache, ws + qb,
+                        v_new, Lnew, cache_seqlens, block_table, bt_stride, max_pages, B, Lq, Hq,
+                        Hkv, D, cache_extent, max_seqlen_k, scale, causal, num_splits, out, lse,
+                        rest ? ws + scratch : nullptr, rest, err_word, dtype, stream);
+}
+
 PA_API size_t pa_fwd_varlen_workspace_size(int B, int total_q, int max_seqlen_q, int Hq,
                                            int Hkv, int D, int max_seqlen_k) {
   if (B <= 0 || total_q <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;

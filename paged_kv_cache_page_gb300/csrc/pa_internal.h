@@ -75,6 +75,22 @@ struct AppendParams {
 // Launchers (each defined in the .cu file that holds its kernel).  They
 // return a cudaError_t from the launch.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+
+// Rotary embedding of a kvcache call's new tokens into scratch copies of q
+// (contiguous [B, Lq, Hq, D]) and k_new ([B, Lnew, Hkv, D]).
+struct RotaryParams {
+  const void* q;
+  int64_t q_sb, q_st, q_sh;
+  const void* k_new;
+  void* q_out;
+  void* k_out;
+  const void* cos;  // [rotary_len, rotary_dim / 2], the q / cache dtype
+  const void* sin;
+  const int32_t* cache_seqlens;
+  int B, Lq, Lnew, Hq, Hkv, D, rotary_dim, rotary_len, interleaved;
+  int32_t* err;
+};
+cudaError_t launch_rotary(const RotaryParams& p, int dtype, cudaStream_t st);
 // `dependent`: launched as a programmatic dependent of the kernel just
 // enqueued on `st` (its blocks may be scheduled while that kernel drains and
 // wait on the device until it has completed and its writes are visible).
