@@ -360,6 +360,33 @@ def secondary_measurements(dev, only=None):
     us_rot = time_calls(rotary, 50, 5, stream)
     res["rotary_decode_b64_ctx4096"] = {"us": round(us_rot, 1), "us_without_rotary": round(us_plain, 1)}
     del w, out
+    # page size 16 vs 256 (the block sizes compared on the flash-attn
+    # integration page): writing a prompt's k/v into the cache (B64 x ctx
+    # 512 / 1024 new tokens, 32 heads x D 128, fp16) and a decode step over
+    # B64 x ctx 4096
+    ps = {}
+    for ctx in (512, 1024):
+        row = []
+        for page in (16, 256):
+            w = wl.prefill_append(batch=64, lnew=ctx, num_heads=32, head_dim=128, old_lo=0,
+                                  old_hi=0, pool=0, dtype="f16", seed=1012, device=dev,
+                                  page_size=page)
+            fn = lambda: pa.pa_append_kv(w["k_cache"], w["v_cache"], w["k_new"], w["v_new"],  # noqa: E731
+                                         w["cache_seqlens"], w["block_table"])
+            row.append(round(time_calls(fn, 30, 5, stream), 1))
+            del w
+        ps[f"append_b64_ctx{ctx}_us"] = {"page16": row[0], "page256": row[1]}
+    row = []
+    for page in (16, 256):
+        w = wl.paged_decode(batch=64, ctx=4096, lnew=1, seed=1013, device=dev, page_size=page)
+        out = torch.empty_like(w["q"])
+        fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
+                                       w["block_table"], k=w["k_new"], v=w["v_new"], out=out,
+                                       return_lse=False)
+        row.append(round(time_calls(fn, 50, 5, stream), 1))
+        del w, out
+    ps["decode_b64_ctx4096_us"] = {"page16": row[0], "page256": row[1]}
+    res["page_size_16_vs_256"] = ps
     # tiny paged decode (launch-latency bound)
     w = wl.tiny_decode(device=dev)
     fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731

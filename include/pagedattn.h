@@ -79,10 +79,18 @@ enum {
   PA_DEVERR_TIMEOUT = 3      /* a pipeline wait exceeded its time limit          */
 };
 
-/* A 4-D cache view.  Paged: [num_pages, 16, Hkv, D] with stride_b = elements
- * between pages, stride_t between the 16 token slots of a page, stride_h
- * between kv heads.  Contiguous (block_table == NULL): [B, capacity, Hkv, D]
- * with stride_b between sequences. */
+/* A 4-D cache view.  Paged: [num_pages, page_size, Hkv, D] with stride_b =
+ * elements between pages, stride_t between the token slots of a page,
+ * stride_h between kv heads.  Contiguous (block_table == NULL):
+ * [B, capacity, Hkv, D] with stride_b between sequences.
+ *
+ * page_size (the paged calls' argument): tokens per page, one of 16, 32, 64,
+ * 128, 256 -- vLLM's 16-token blocks and the 256-token pages flash-attention
+ * required, which vLLM #3010 "Introduce flash-attn" compares (cache-write cost
+ * at context 512 / 1024).  Ignored when block_table == NULL; any other value
+ * with a block table returns PA_ERR_UNSUPPORTED.  Position pos of sequence b
+ * is in page block_table[b * bt_stride + pos / page_size], slot
+ * pos % page_size. */
 typedef struct {
   void* ptr;
   int64_t stride_b;
@@ -95,7 +103,7 @@ typedef struct {
  *
  * For every b < B, i < Lnew, kv head g: position pos = cache_seqlens[b] + i
  * receives k_new[b, i, g, :] (and v_new likewise) at page
- * block_table[b * bt_stride + pos / 16], slot pos % 16; or, with
+ * block_table[b * bt_stride + pos / page_size], slot pos % page_size; or, with
  * block_table == NULL, at row [b, pos] of a contiguous cache.  The k=/v=
  * append of flash_attn_with_kvcache (flash-attention #824, reproduction
  * snippet and the reply noting that the call allocates nothing and writes
@@ -105,15 +113,15 @@ typedef struct {
  *   block_table   int32 [B, >= max_pages] rows of stride bt_stride, or NULL.
  *   cache_extent  paged: number of pages in the pool; contiguous: capacity
  *                 (tokens) of each sequence.
- * Positions outside the table (pos / 16 >= max_pages) or the capacity, and
+ * Positions outside the table (pos / page_size >= max_pages) or the capacity, and
  * out-of-pool pages, are skipped and reported in err_word.  Appends of two
  * sequences that share a physical page race (the caller's responsibility).
  */
 PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                         const void* v_new, const int32_t* cache_seqlens,
-                        const int32_t* block_table, int64_t bt_stride, int max_pages, int B,
-                        int Lnew, int Hkv, int D, int64_t cache_extent, int dtype,
-                        int32_t* err_word, pa_stream_t stream);
+                        const int32_t* block_table, int64_t bt_stride, int max_pages,
+                        int page_size, int B, int Lnew, int Hkv, int D, int64_t cache_extent,
+                        int dtype, int32_t* err_word, pa_stream_t stream);
 
 /*
  * pa_fwd_kvcache -- flash_attn_with_kvcache forward: decode, multi-query
@@ -132,7 +140,8 @@ PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_ne
  *   k_new/v_new  [B, Lnew, Hkv, D] contiguous, or NULL with Lnew == 0.
  *   cache_seqlens int32 [B] (device): tokens already cached.
  *   block_table  int32 [B, >= max_pages] (row stride bt_stride) or NULL for a
- *                contiguous cache; entries past ceil(Lk_b/16) are never read.
+ *                contiguous cache; entries past ceil(Lk_b/page_size) are never
+ *                read.  page_size: see pa_tensor4.
  *   cache_extent paged: pages in the pool; contiguous: tokens per sequence.
  *   max_seqlen_k host-known upper bound of Lk_b (a capacity, never read back).
  *   scale        softmax scale (e.g. 1/sqrt(D)).
@@ -148,8 +157,9 @@ PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_ne
 PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
                           pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                           const void* v_new, int Lnew, const int32_t* cache_seqlens,
-                          const int32_t* block_table, int64_t bt_stride, int max_pages, int B,
-                          int Lq, int Hq, int Hkv, int D, int64_t cache_extent, int max_seqlen_k,
+                          const int32_t* block_table, int64_t bt_stride, int max_pages,
+                          int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                          int64_t cache_extent, int max_seqlen_k,
                           float scale, int causal, int num_splits, void* out, float* lse,
                           void* workspace, size_t workspace_bytes, int32_t* err_word, int dtype,
                           pa_stream_t stream);
@@ -192,8 +202,9 @@ PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int6
                                  pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                                  const void* v_new, int Lnew, const int32_t* cache_seqlens,
                                  const int32_t* block_table, int64_t bt_stride, int max_pages,
-                                 int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
-                                 int max_seqlen_k, const void* rotary_cos, const void* rotary_sin,
+                                 int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                                 int64_t cache_extent, int max_seqlen_k, const void* rotary_cos,
+                                 const void* rotary_sin,
                                  int rotary_len, int rotary_dim, int rotary_interleaved,
                                  float scale, int causal, int num_splits, void* out, float* lse,
                                  void* workspace, size_t workspace_bytes, int32_t* err_word,
@@ -231,6 +242,7 @@ PA_API int pa_fwd_kvcache_noalloc(const void* q, int64_t q_sb, int64_t q_st, int
                                   pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                                   const void* v_new, int Lnew, const int32_t* cache_seqlens,
                                   const int32_t* block_table, int64_t bt_stride, int max_pages,
+                                  int page_size,
                                   int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
                                   int max_seqlen_k, float scale, int causal, int num_splits,
                                   void* out, float* lse, int32_t* err_word, int dtype,
@@ -255,7 +267,8 @@ PA_API int pa_fwd_kvcache_noalloc(const void* q, int64_t q_sb, int64_t q_st, int
 PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_tensor4 k_cache,
                                  pa_tensor4 v_cache, const int32_t* cu_seqlens_q,
                                  const int32_t* seqlens_k, const int32_t* block_table,
-                                 int64_t bt_stride, int max_pages, int B, int total_q,
+                                 int64_t bt_stride, int max_pages, int page_size, int B,
+                                 int total_q,
                                  int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
                                  int64_t num_pages, float scale, int causal, void* out,
                                  float* lse, void* workspace, size_t workspace_bytes,

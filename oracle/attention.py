@@ -6,11 +6,13 @@ leg may import this module.  It shares no code with the CUDA library.
 Definition followed (restated from the pages, see the package docstring for
 the page list):
 
-* Paged cache layout ``[num_pages, P, Hkv, D]`` with P = 16 tokens per page;
-  ``block_table[b, j]`` is the physical page holding logical page j of
-  sequence b -- [p1] "Add support for small page sizes", reproduction snippet
-  (``key_cache = [num_blocks, block_size, num_heads, head_dim]``,
-  ``block_tables = [bs, cdiv(seq_len, block_size)]``).
+* Paged cache layout ``[num_pages, P, Hkv, D]`` with P tokens per page (the
+  cache's second dimension: 16 in the configurations, 256 in the comparison
+  of [p4]); ``block_table[b, j]`` is the physical page holding logical page j
+  of sequence b -- [p1] "Add support for small page sizes", reproduction
+  snippet (``key_cache = [num_blocks, block_size, num_heads, head_dim]``,
+  ``block_tables = [bs, cdiv(seq_len, block_size)]``); [p4] "Introduce
+  flash-attn", the block size 16 vs 256 comparison.
 * Non-paged cache ``[B, max_len, Hkv, D]`` whose valid length per sequence is
   ``cache_seqlens[b]`` -- [p3] "Inappropriate Number of Splits ...", opening
   report (cache preallocated to 131072 tokens, real length from
@@ -87,8 +89,8 @@ def logical_kv(k_cache, v_cache, b, old_len, k_new=None, v_new=None, block_table
         k_old = k_cache[b, :old_len]
         v_old = v_cache[b, :old_len]
     else:
-        k_old = gather_pages(k_cache, block_table[b], old_len)
-        v_old = gather_pages(v_cache, block_table[b], old_len)
+        k_old = gather_pages(k_cache, block_table[b], old_len, k_cache.shape[1])
+        v_old = gather_pages(v_cache, block_table[b], old_len, v_cache.shape[1])
     k_old = np.asarray(k_old, dtype=np.float64)
     v_old = np.asarray(v_old, dtype=np.float64)
     if k_new is None:
@@ -130,7 +132,7 @@ def attend_rows(q, k, v, scale, causal):
 
 
 def append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table=None,
-              page_size=PAGE_SIZE):
+              page_size=None):
     """Bit copy of the new tokens into the cache; returns updated copies.
 
     Works on any dtype (pass integer bit views for a bit-exact check).  New
@@ -140,6 +142,8 @@ def append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table=None,
     """
     kc = np.array(k_cache, copy=True)
     vc = np.array(v_cache, copy=True)
+    if page_size is None:
+        page_size = kc.shape[1]
     bsz, lnew = k_new.shape[0], k_new.shape[1]
     for b in range(bsz):
         for i in range(lnew):
@@ -198,8 +202,10 @@ def fwd_varlen(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, scale=
         if q1 == q0:
             continue
         lk = int(seqlens_k[b])
-        kk = np.asarray(gather_pages(k_cache, block_table[b], lk), dtype=np.float64)
-        vv = np.asarray(gather_pages(v_cache, block_table[b], lk), dtype=np.float64)
+        kk = np.asarray(gather_pages(k_cache, block_table[b], lk, k_cache.shape[1]),
+                        dtype=np.float64)
+        vv = np.asarray(gather_pages(v_cache, block_table[b], lk, v_cache.shape[1]),
+                        dtype=np.float64)
         o_b, lse_b = attend_rows(q[q0:q1], kk, vv, scale, causal)
         out[q0:q1] = o_b
         lse[:, q0:q1] = lse_b

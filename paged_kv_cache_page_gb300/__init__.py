@@ -53,23 +53,24 @@ _vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, cty
 
 _SIGNATURES = {
     "pa_append_kv": (_i32, [pa_tensor4, pa_tensor4, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
-                            _i32, _i32, _i64, _i32, _vp, _vp]),
+                            _i32, _i32, _i32, _i64, _i32, _vp, _vp]),
     "pa_fwd_kvcache": (_i32, [_vp, _i64, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp, _i32,
-                              _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i32,
-                              _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
+                              _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
+                              _i32, _f32, _i32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
     "pa_fwd_kvcache_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_fwd_kvcache_rotary": (_i32, [_vp, _i64, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp,
                                      _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32,
-                                     _i64, _i32, _vp, _vp, _i32, _i32, _i32, _f32, _i32, _i32,
-                                     _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
+                                     _i32, _i64, _i32, _vp, _vp, _i32, _i32, _i32, _f32, _i32,
+                                     _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
     "pa_fwd_kvcache_rotary_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                                    _i32]),
     "pa_fwd_kvcache_noalloc": (_i32, [_vp, _i64, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp,
                                       _i32, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _i32,
-                                      _i64, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _i32, _vp]),
+                                      _i32, _i64, _i32, _f32, _i32, _i32, _vp, _vp, _vp, _i32,
+                                      _vp]),
     "pa_fwd_varlen_unified": (_i32, [_vp, _i64, _i64, pa_tensor4, pa_tensor4, _vp, _vp, _vp,
-                                     _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i64,
-                                     _f32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
+                                     _i64, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                     _i64, _f32, _i32, _vp, _vp, _vp, _sz, _vp, _i32, _vp]),
     "pa_fwd_varlen_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_split_combine": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _i32,
                                 _vp]),
@@ -110,6 +111,12 @@ def _cuda(*ts):
             raise ValueError("pagedattn tensors must be on a CUDA device")
 
 
+def _page_size(k_cache, block_table):
+    """Tokens per page of a paged cache ``[num_pages, page_size, Hkv, D]``
+    (ignored by the library for a contiguous cache)."""
+    return k_cache.shape[1] if block_table is not None else PAGE_SIZE
+
+
 def _stream(t):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
@@ -143,8 +150,9 @@ def pa_append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table=None
     else:
         extent, max_pages, bt_stride = k_cache.shape[1], 0, 0
     _check(lib.pa_append_kv(_t4(k_cache), _t4(v_cache), _ptr(k_new), _ptr(v_new),
-                            _ptr(cache_seqlens), _ptr(block_table), bt_stride, max_pages, B, lnew,
-                            hkv, d, extent, _dtype(k_cache), _ptr(err), _stream(k_cache)))
+                            _ptr(cache_seqlens), _ptr(block_table), bt_stride, max_pages,
+                            _page_size(k_cache, block_table), B, lnew, hkv, d, extent,
+                            _dtype(k_cache), _ptr(err), _stream(k_cache)))
 
 
 def fwd_kvcache_workspace_size(B, Lq, Hq, Hkv, D, max_seqlen_k, num_splits=0):
@@ -175,7 +183,7 @@ def pa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, k=None,
         v = v.contiguous()
     if block_table is not None:
         extent, max_pages, bt_stride = k_cache.shape[0], block_table.shape[1], block_table.stride(0)
-        cap = max_pages * PAGE_SIZE
+        cap = max_pages * k_cache.shape[1]
     else:
         extent, max_pages, bt_stride = k_cache.shape[1], 0, 0
         cap = extent
@@ -198,8 +206,9 @@ def pa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, k=None,
         ws_len = workspace.numel() * workspace.element_size()
         _check(lib.pa_fwd_kvcache_rotary(
             _ptr(q), q.stride(0), q.stride(1), q.stride(2), _t4(k_cache), _t4(v_cache), _ptr(k),
-            _ptr(v), lnew, _ptr(cache_seqlens), _ptr(block_table), bt_stride, max_pages, B, lq,
-            hq, hkv, d, extent, max_seqlen_k, _ptr(rotary_cos), _ptr(rotary_sin),
+            _ptr(v), lnew, _ptr(cache_seqlens), _ptr(block_table), bt_stride, max_pages,
+            _page_size(k_cache, block_table), B, lq, hq, hkv, d, extent, max_seqlen_k,
+            _ptr(rotary_cos), _ptr(rotary_sin),
             rotary_cos.shape[0], 2 * rotary_cos.shape[1], int(bool(rotary_interleaved)),
             float(scale), int(bool(causal)), int(num_splits), _ptr(out), _ptr(lse),
             _ptr(workspace), ws_len, _ptr(err), _dtype(q), _stream(q)))
@@ -210,7 +219,8 @@ def pa_fwd_kvcache(q, k_cache, v_cache, cache_seqlens, block_table=None, k=None,
     ws_len = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.pa_fwd_kvcache(_ptr(q), q.stride(0), q.stride(1), q.stride(2), _t4(k_cache),
                               _t4(v_cache), _ptr(k), _ptr(v), lnew, _ptr(cache_seqlens),
-                              _ptr(block_table), bt_stride, max_pages, B, lq, hq, hkv, d, extent,
+                              _ptr(block_table), bt_stride, max_pages,
+                              _page_size(k_cache, block_table), B, lq, hq, hkv, d, extent,
                               max_seqlen_k, float(scale), int(bool(causal)), int(num_splits),
                               _ptr(out), _ptr(lse), _ptr(workspace), ws_len, _ptr(err),
                               _dtype(q), _stream(q)))
@@ -234,7 +244,7 @@ def pa_fwd_kvcache_noalloc(q, k_cache, v_cache, cache_seqlens, out, block_table=
     lnew = 0 if k is None else k.shape[1]
     if block_table is not None:
         extent, max_pages, bt_stride = k_cache.shape[0], block_table.shape[1], block_table.stride(0)
-        cap = max_pages * PAGE_SIZE
+        cap = max_pages * k_cache.shape[1]
     else:
         extent, max_pages, bt_stride = k_cache.shape[1], 0, 0
         cap = extent
@@ -245,7 +255,8 @@ def pa_fwd_kvcache_noalloc(q, k_cache, v_cache, cache_seqlens, out, block_table=
     _check(lib.pa_fwd_kvcache_noalloc(_ptr(q), q.stride(0), q.stride(1), q.stride(2),
                                       _t4(k_cache), _t4(v_cache), _ptr(k), _ptr(v), lnew,
                                       _ptr(cache_seqlens), _ptr(block_table), bt_stride,
-                                      max_pages, B, lq, hq, hkv, d, extent, max_seqlen_k,
+                                      max_pages, _page_size(k_cache, block_table), B, lq, hq, hkv,
+                                      d, extent, max_seqlen_k,
                                       float(scale), int(bool(causal)), int(num_splits),
                                       _ptr(out), _ptr(lse), _ptr(err), _dtype(q), _stream(q)))
     return out, lse
@@ -278,7 +289,8 @@ def pa_fwd_varlen_unified(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_ta
     _check(lib.pa_fwd_varlen_unified(_ptr(q), q.stride(0), q.stride(1), _t4(k_cache),
                                      _t4(v_cache), _ptr(cu_seqlens_q), _ptr(seqlens_k),
                                      _ptr(block_table), block_table.stride(0),
-                                     block_table.shape[1], B, total_q, max_seqlen_q, max_seqlen_k,
+                                     block_table.shape[1], k_cache.shape[1], B, total_q,
+                                     max_seqlen_q, max_seqlen_k,
                                      hq, hkv, d, k_cache.shape[0], float(scale),
                                      int(bool(causal)), _ptr(out), _ptr(lse), _ptr(workspace),
                                      ws_len, _ptr(err), _dtype(q), _stream(q)))

@@ -33,6 +33,19 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tokens per page of a paged cache: 16 << shift with shift in [0, 4] (16 to 256
+// tokens, the 16-token pages of vLLM and the 256-token ones flash-attention
+// required, vLLM #3010).  The kernels move 16-token boxes; a page holds
+// 1 << shift of them.  Returns false for other sizes.
+bool page_shift_of(int page_size, int* shift) {
+  for (int s = 0; s <= 4; ++s)
+    if (page_size == (kPage << s)) {
+      *shift = s;
+      return true;
+    }
+  return false;
+}
 bool mult8(int64_t s) { return s > 0 && (s % 8) == 0; }
 
 // Split-KV planning constants.  The host only fixes a cap on splits per
@@ -215,9 +228,9 @@ PA_API int pa_version(void) { return 100; }
 
 PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                         const void* v_new, const int32_t* cache_seqlens,
-                        const int32_t* block_table, int64_t bt_stride, int max_pages, int B,
-                        int Lnew, int Hkv, int D, int64_t cache_extent, int dtype,
-                        int32_t* err_word, pa_stream_t stream) {
+                        const int32_t* block_table, int64_t bt_stride, int max_pages,
+                        int page_size, int B, int Lnew, int Hkv, int D, int64_t cache_extent,
+                        int dtype, int32_t* err_word, pa_stream_t stream) {
   int rc = check_common(dtype, D, Hkv, Hkv);
   if (rc) return rc;
   if (B < 0 || Lnew < 0) return fail(PA_ERR_INVALID_ARG, "negative B or Lnew");
@@ -230,7 +243,11 @@ PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_ne
   if (cache_extent < 1) return fail(PA_ERR_INVALID_ARG, "cache_extent must be >= 1");
   if (block_table != nullptr && (max_pages < 1 || bt_stride < max_pages))
     return fail(PA_ERR_INVALID_ARG, "block table needs max_pages >= 1 and bt_stride >= max_pages");
+  int shift = 0;
+  if (block_table != nullptr && !page_shift_of(page_size, &shift))
+    return fail(PA_ERR_UNSUPPORTED, "page_size must be 16, 32, 64, 128 or 256");
   AppendParams p{};
+  p.page_shift = shift;
   p.k_cache = k_cache.ptr;
   p.v_cache = v_cache.ptr;
   p.k_sb = k_cache.stride_b; p.k_st = k_cache.stride_t; p.k_sh = k_cache.stride_h;
@@ -279,8 +296,9 @@ PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int6
                                  pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                                  const void* v_new, int Lnew, const int32_t* cache_seqlens,
                                  const int32_t* block_table, int64_t bt_stride, int max_pages,
-                                 int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
-                                 int max_seqlen_k, const void* rotary_cos, const void* rotary_sin,
+                                 int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                                 int64_t cache_extent, int max_seqlen_k, const void* rotary_cos,
+                                 const void* rotary_sin,
                                  int rotary_len, int rotary_dim, int rotary_interleaved,
                                  float scale, int causal, int num_splits, void* out, float* lse,
                                  void* workspace, size_t workspace_bytes, int32_t* err_word,
@@ -324,8 +342,9 @@ PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int6
   if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
   const size_t rest = workspace_bytes - scratch;
   return pa_fwd_kvcache(ws, (int64_t)Lq * Hq * D, (int64_t)Hq * D, D, k_cache, v_cache, ws + qb,
-                        v_new, Lnew, cache_seqlens, block_table, bt_stride, max_pages, B, Lq, Hq,
-                        Hkv, D, cache_extent, max_seqlen_k, scale, causal, num_splits, out, lse,
+                        v_new, Lnew, cache_seqlens, block_table, bt_stride, max_pages, page_size,
+                        B, Lq, Hq, Hkv, D, cache_extent, max_seqlen_k, scale, causal, num_splits,
+                        out, lse,
                         rest ? ws + scratch : nullptr, rest, err_word, dtype, stream);
 }
 
@@ -340,8 +359,9 @@ PA_API size_t pa_fwd_varlen_workspace_size(int B, int total_q, int max_seqlen_q,
 PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
                           pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                           const void* v_new, int Lnew, const int32_t* cache_seqlens,
-                          const int32_t* block_table, int64_t bt_stride, int max_pages, int B,
-                          int Lq, int Hq, int Hkv, int D, int64_t cache_extent, int max_seqlen_k,
+                          const int32_t* block_table, int64_t bt_stride, int max_pages,
+                          int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                          int64_t cache_extent, int max_seqlen_k,
                           float scale, int causal, int num_splits, void* out, float* lse,
                           void* workspace, size_t workspace_bytes, int32_t* err_word, int dtype,
                           pa_stream_t stream) {
@@ -357,10 +377,15 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   if (cache_extent < 1) return fail(PA_ERR_INVALID_ARG, "cache_extent must be >= 1");
   if (block_table != nullptr && (max_pages < 1 || bt_stride < max_pages))
     return fail(PA_ERR_INVALID_ARG, "block table needs max_pages >= 1 and bt_stride >= max_pages");
+  int shift = 0;
+  if (block_table != nullptr && !page_shift_of(page_size, &shift))
+    return fail(PA_ERR_UNSUPPORTED, "page_size must be 16, 32, 64, 128 or 256");
+  const int64_t page_rows = (int64_t)kPage << shift;
   if (Lq == 0) {
     if (Lnew == 0) return PA_OK;
     return pa_append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table, bt_stride,
-                        max_pages, B, Lnew, Hkv, D, cache_extent, dtype, err_word, stream);
+                        max_pages, page_size, B, Lnew, Hkv, D, cache_extent, dtype, err_word,
+                        stream);
   }
   if (q == nullptr || out == nullptr) return fail(PA_ERR_INVALID_ARG, "q and out must be non-NULL");
   if (!aligned16(q) || !aligned16(out))
@@ -380,7 +405,8 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     // longer ones as 128-row tiles of one head.
     if (Lnew > 0) {
       rc = pa_append_kv(k_cache, v_cache, k_new, v_new, cache_seqlens, block_table, bt_stride,
-                        max_pages, B, Lnew, Hkv, D, cache_extent, dtype, err_word, stream);
+                        max_pages, page_size, B, Lnew, Hkv, D, cache_extent, dtype, err_word,
+                        stream);
       if (rc) return rc;
     }
     const bool pack = rows <= kEngineMaxRows && (kEngineMaxRows % G) == 0;
@@ -394,10 +420,10 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     if (!encode_map(&tq1, q, dtype, D, Hq, Lq, B, q_sh, q_st, q_sb, 64, 1, 128) ||
         !encode_map(&tq2, q, dtype, D, Hq, Lq, B, q_sh, q_st, q_sb, 64, pack ? G : 1,
                     pack ? kEngineMaxRows / G : 128) ||
-        !encode_map(&tk, k_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
+        !encode_map(&tk, k_cache.ptr, dtype, D, Hkv, paged_p ? page_rows : cache_extent,
                     paged_p ? cache_extent : B, k_cache.stride_h, k_cache.stride_t,
                     k_cache.stride_b, 64, 1, kPage) ||
-        !encode_map(&tv, v_cache.ptr, dtype, D, Hkv, paged_p ? kPage : cache_extent,
+        !encode_map(&tv, v_cache.ptr, dtype, D, Hkv, paged_p ? page_rows : cache_extent,
                     paged_p ? cache_extent : B, v_cache.stride_h, v_cache.stride_t,
                     v_cache.stride_b, 64, 1, kPage))
       return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for q or the caches");
@@ -410,6 +436,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     ep.block_table = block_table;
     ep.bt_stride = bt_stride;
     ep.max_pages = paged_p ? max_pages : 0;
+    ep.page_shift = shift;
     ep.extent = cache_extent;
     ep.B = B; ep.Lq = Lq; ep.Hq = Hq; ep.Hkv = Hkv; ep.G = G;
     ep.max_seqlen_k = max_seqlen_k;
@@ -456,7 +483,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
 
   CUtensorMap tmk, tmv;
   const bool paged = block_table != nullptr;
-  const int64_t dim2 = paged ? kPage : cache_extent;
+  const int64_t dim2 = paged ? page_rows : cache_extent;
   const int64_t dim3 = paged ? cache_extent : B;
   if (!encode_cache_map(&tmk, k_cache.ptr, dtype, D, Hkv, dim2, dim3, k_cache.stride_h,
                         k_cache.stride_t, k_cache.stride_b, D, kPage, false) ||
@@ -479,6 +506,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   p.block_table = block_table;
   p.bt_stride = bt_stride;
   p.max_pages = paged ? max_pages : 0;
+  p.page_shift = shift;
   p.extent = cache_extent;
   p.cache_seqlens = cache_seqlens;
   p.cu_seqlens_q = nullptr;
@@ -520,7 +548,8 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
 PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_tensor4 k_cache,
                                  pa_tensor4 v_cache, const int32_t* cu_seqlens_q,
                                  const int32_t* seqlens_k, const int32_t* block_table,
-                                 int64_t bt_stride, int max_pages, int B, int total_q,
+                                 int64_t bt_stride, int max_pages, int page_size, int B,
+                                 int total_q,
                                  int max_seqlen_q, int max_seqlen_k, int Hq, int Hkv, int D,
                                  int64_t num_pages, float scale, int causal, void* out,
                                  float* lse, void* workspace, size_t workspace_bytes,
@@ -538,6 +567,9 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
   if (!mult8(q_st) || !mult8(q_sh)) return fail(PA_ERR_INVALID_ARG, "q strides multiples of 8");
   if (max_pages < 1 || bt_stride < max_pages || num_pages < 1)
     return fail(PA_ERR_INVALID_ARG, "block table / pool sizes");
+  int shift = 0;
+  if (!page_shift_of(page_size, &shift))
+    return fail(PA_ERR_UNSUPPORTED, "page_size must be 16, 32, 64, 128 or 256");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale");
   if (B > kEngineMaxB) return fail(PA_ERR_UNSUPPORTED, "more than %d sequences", kEngineMaxB);
   const int G = Hq / Hkv;
@@ -555,9 +587,9 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
   if (!encode_map(&tq1, q, dtype, D, Hq, total_q, 1, q_sh, q_st, q_st * total_q, 64, 1, 128) ||
       !encode_map(&tq2, q, dtype, D, Hq, total_q, 1, q_sh, q_st, q_st * total_q, 64,
                   pack ? G : 1, pack ? kEngineMaxRows / G : 128) ||
-      !encode_map(&tk, k_cache.ptr, dtype, D, Hkv, kPage, num_pages, k_cache.stride_h,
+      !encode_map(&tk, k_cache.ptr, dtype, D, Hkv, page_size, num_pages, k_cache.stride_h,
                   k_cache.stride_t, k_cache.stride_b, 64, 1, kPage) ||
-      !encode_map(&tv, v_cache.ptr, dtype, D, Hkv, kPage, num_pages, v_cache.stride_h,
+      !encode_map(&tv, v_cache.ptr, dtype, D, Hkv, page_size, num_pages, v_cache.stride_h,
                   v_cache.stride_t, v_cache.stride_b, 64, 1, kPage))
     return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for q or the caches");
   const int grid = engine_grid();
@@ -569,6 +601,7 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
   ep.block_table = block_table;
   ep.bt_stride = bt_stride;
   ep.max_pages = max_pages;
+  ep.page_shift = shift;
   ep.extent = num_pages;
   ep.B = B; ep.Lq = 0; ep.Hq = Hq; ep.Hkv = Hkv; ep.G = G;
   ep.max_seqlen_k = max_seqlen_k;

@@ -14,7 +14,7 @@ namespace {
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const int chunks = p.D / 8;  // 16-byte chunks per row
   const long long total = (long long)p.B * p.Lnew * p.Hkv * chunks;
-  CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, p.k_sb, p.k_st};
+  CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, p.k_sb, p.k_st, p.page_shift};
   for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const int c = (int)(idx % chunks);
@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const int old = __ldg(p.cache_seqlens + b);
     const long long pos = (long long)old + i;
     const bool len_ok = old >= 0 &&
-                        (p.block_table != nullptr ? (pos / kPage) < p.max_pages : pos < p.extent);
+                        (p.block_table != nullptr ? ((pos / kPage) >> p.page_shift) < p.max_pages
+                                                  : pos < p.extent);
     if (!len_ok) {
       if (g == 0 && c == 0) report(p.err, PA_DEVERR_LENGTH, b, (int)pos);
       continue;

@@ -86,7 +86,8 @@ __device__ __forceinline__ SeqInfo seq_info(const DecodeParams& p, int b, bool r
   }
   bool bad = si.old < 0 || si.lk < 0 || si.lk > p.max_seqlen_k || si.qlen < 0;
   if (p.block_table != nullptr) {
-    bad = bad || (int64_t)(si.lk + kPage - 1) / kPage > p.max_pages;
+    bad = bad || (((int64_t)(si.lk + kPage - 1) / kPage + (1 << p.page_shift) - 1) >> p.page_shift) >
+                     p.max_pages;
   } else {
     bad = bad || (int64_t)si.lk > p.extent;
   }
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads, 2)
     // table load.  Lanes 0-3 issue the K boxes and lanes 4-7 the V boxes of
     // a stage's pages.
     const uint64_t pol = l2_policy_evict_first();
-    CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, p.k_sb, p.k_st};
+    CacheGeom geom{p.block_table, p.bt_stride, p.max_pages, p.extent, p.k_sb, p.k_st, p.page_shift};
     int stage = 0;
     uint32_t phase = 0;
     bool failed = false;

@@ -112,7 +112,8 @@ __device__ __forceinline__ SeqI seq_of(const EngineParams& p, int b, bool rep) {
   }
   bool bad = old < 0 || s.lk < 0 || s.lk > p.max_seqlen_k || s.qlen < 0;
   if (p.block_table != nullptr)
-    bad = bad || (int64_t)(s.lk + kPage - 1) / kPage > p.max_pages;
+    bad = bad || (((int64_t)(s.lk + kPage - 1) / kPage + (1 << p.page_shift) - 1) >> p.page_shift) >
+                     p.max_pages;
   else
     bad = bad || (int64_t)s.lk > p.extent;
   if (bad) {
@@ -441,9 +442,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg_begin = it.k0 / kPage;
       const int pg_end = (it.k1 + kPage - 1) / kPage;
       const int32_t* trow = paged ? p.block_table + (int64_t)it.b * p.bt_stride : nullptr;
-      auto load_batch = [&](int batch) -> int {  // raw entry of page pg_begin + 32*batch + lane
+      // raw table entry of 16-token box pg_begin + 32*batch + lane (its page:
+      // entry box >> page_shift)
+      auto load_batch = [&](int batch) -> int {
         const int lp = pg_begin + 32 * batch + lane;
-        return (paged && lp < pg_end && lp < p.max_pages) ? __ldg(trow + lp) : 0;
+        const int entry = lp >> p.page_shift;
+        return (paged && lp < pg_end && entry < p.max_pages) ? __ldg(trow + entry) : 0;
       };
       int cur = load_batch(0);
       int nxt = (it.ntiles > 4) ? load_batch(1) : 0;
@@ -480,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int lp = pg0 + i;
           bool ok;
           if (paged) {
-            ok = lp < p.max_pages && raw >= 0 && (int64_t)raw < p.extent;
-            c2[i] = 0;
+            ok = (lp >> p.page_shift) < p.max_pages && raw >= 0 && (int64_t)raw < p.extent;
+            c2[i] = ok ? (lp & ((1 << p.page_shift) - 1)) * kPage : 0;
             c3[i] = ok ? raw : 0;
           } else {
             ok = (int64_t)lp * kPage < p.extent;

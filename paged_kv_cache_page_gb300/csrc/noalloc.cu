@@ -69,7 +69,8 @@ PA_API int pa_fwd_kvcache_noalloc(const void* q, int64_t q_sb, int64_t q_st, int
                                   pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
                                   const void* v_new, int Lnew, const int32_t* cache_seqlens,
                                   const int32_t* block_table, int64_t bt_stride, int max_pages,
-                                  int B, int Lq, int Hq, int Hkv, int D, int64_t cache_extent,
+                                  int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                                  int64_t cache_extent,
                                   int max_seqlen_k, float scale, int causal, int num_splits,
                                   void* out, float* lse, int32_t* err_word, int dtype,
                                   pa_stream_t stream) {
@@ -90,7 +91,8 @@ PA_API int pa_fwd_kvcache_noalloc(const void* q, int64_t q_sb, int64_t q_st, int
                            cudaGetErrorString(e));
   }
   return pa_fwd_kvcache(q, q_sb, q_st, q_sh, k_cache, v_cache, k_new, v_new, Lnew,
-                        cache_seqlens, block_table, bt_stride, max_pages, B, Lq, Hq, Hkv, D,
+                        cache_seqlens, block_table, bt_stride, max_pages, page_size, B, Lq, Hq,
+                        Hkv, D,
                         cache_extent, max_seqlen_k, scale, causal, num_splits, out, lse, scratch,
                         need, err_word, dtype, stream);
 }

@@ -189,11 +189,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 }
 
 // ---------------------------------------------------------------- page resolution
-// Where logical page `lp` of sequence `b` lives, as TMA coordinates
-// (row coordinate c2, page-or-sequence coordinate c3) and as an element
-// offset of its first token slot for head 0.  The page is resolved absolutely
-// for every iteration (never by a delta from the previous page), and the
-// table is never indexed at or beyond `max_pages`.
+// Where the 16-token box `lp` (tokens [16 lp, 16 lp + 16)) of sequence `b`
+// lives, as TMA coordinates (row coordinate c2, page-or-sequence coordinate
+// c3) and as an element offset of its first token slot for head 0.  Pages of
+// P = 16 << page_shift tokens hold 1 << page_shift boxes: the box is in the
+// page of table entry lp >> page_shift, at row 16 (lp mod (1 << page_shift)).
+// The page is resolved absolutely for every iteration (never by a delta from
+// the previous page), and the table is never indexed at or beyond
+// `max_pages`.
 struct PageRef {
   int c2, c3;
   int64_t elem_off;  // offset of slot 0, head 0 (element units) in the K cache view
@@ -206,19 +209,21 @@ struct CacheGeom {
   int max_pages;      // table width (paged)
   int64_t extent;     // pages in pool (paged) or tokens per sequence (contiguous)
   int64_t sb, st;     // element strides of the K cache (V uses its own strides)
+  int page_shift;     // log2(page size / 16) (paged)
 };
 
 __device__ __forceinline__ PageRef resolve_page(const CacheGeom& g, int b, int lp) {
   PageRef r;
   if (g.block_table != nullptr) {
     int phys = 0;
-    bool ok = lp >= 0 && lp < g.max_pages;
-    if (ok) phys = __ldg(g.block_table + (int64_t)b * g.bt_stride + lp);
+    const int entry = lp >> g.page_shift;
+    bool ok = lp >= 0 && entry < g.max_pages;
+    if (ok) phys = __ldg(g.block_table + (int64_t)b * g.bt_stride + entry);
     ok = ok && phys >= 0 && (int64_t)phys < g.extent;
     if (!ok) phys = 0;
-    r.c2 = 0;
+    r.c2 = ok ? (lp & ((1 << g.page_shift) - 1)) * kPage : 0;
     r.c3 = phys;
-    r.elem_off = (int64_t)phys * g.sb;
+    r.elem_off = (int64_t)phys * g.sb + (int64_t)r.c2 * g.st;
     r.ok = ok;
   } else {
     // Rows past the capacity in the last box are zero-filled by the TMA unit

@@ -21,6 +21,7 @@ struct EngineParams {
   const int32_t* block_table;    // null: contiguous cache
   int64_t bt_stride;
   int max_pages;
+  int page_shift;                // log2(page size / 16): 16-token boxes per table entry
   int64_t extent;                // pages in pool, or tokens per sequence
   int B, Lq, Hq, Hkv, G, max_seqlen_k, total_q;
   int pack_rows;   // sequences with q_len * G <= pack_rows run as packed items (one per kv head

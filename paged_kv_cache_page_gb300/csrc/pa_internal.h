@@ -31,6 +31,7 @@ struct DecodeParams {
   const int32_t* block_table;  // null: contiguous cache
   int64_t bt_stride;
   int max_pages;
+  int page_shift;  // log2(page size / 16): 16-token boxes per table entry = 1 << page_shift
   int64_t extent;  // pages in pool, or tokens per sequence (contiguous)
   const int32_t* cache_seqlens;  // kvcache mode
   const int32_t* cu_seqlens_q;   // varlen mode (non-null selects it)
@@ -67,6 +68,7 @@ struct AppendParams {
   const int32_t* block_table;
   int64_t bt_stride;
   int max_pages;
+  int page_shift;  // log2(page size / 16)
   int64_t extent;
   int B, Lnew, Hkv, D;
   int32_t* err;

@@ -56,7 +56,8 @@ def _distinct_tables(pages_per_seq, pool, g, device):
 
 
 def paged_decode(batch, ctx, num_q_heads=32, num_kv_heads=32, head_dim=128, dtype="f16",
-                 lnew=0, seed=1002, device="cpu", lens=None, dist="normal", pool=None):
+                 lnew=0, seed=1002, device="cpu", lens=None, dist="normal", pool=None,
+                 page_size=PAGE_SIZE):
     """Paged decode: Lq = 1 (or ``lnew`` new tokens with in-kernel append).
 
     Every sequence holds ``ctx`` keys after the call: ``cache_seqlens = ctx - lnew``
@@ -69,12 +70,12 @@ def paged_decode(batch, ctx, num_q_heads=32, num_kv_heads=32, head_dim=128, dtyp
     g = _gen(seed, device)
     if lens is None:
         lens = [ctx] * batch
-    pages = [-(-int(l) // PAGE_SIZE) for l in lens]
+    pages = [-(-int(l) // page_size) for l in lens]
     num_pages = sum(pages) if pool is None else pool
     table = _distinct_tables(pages, num_pages, torch.Generator().manual_seed(seed), device)
     lq = max(1, lnew)
-    k_cache = _values((num_pages, PAGE_SIZE, num_kv_heads, head_dim), dt, dist, g, device)
-    v_cache = _values((num_pages, PAGE_SIZE, num_kv_heads, head_dim), dt, dist, g, device)
+    k_cache = _values((num_pages, page_size, num_kv_heads, head_dim), dt, dist, g, device)
+    v_cache = _values((num_pages, page_size, num_kv_heads, head_dim), dt, dist, g, device)
     q = _values((batch, lq, num_q_heads, head_dim), dt, dist, g, device)
     if lnew > 0:
         k_new = _values((batch, lnew, num_kv_heads, head_dim), dt, dist, g, device)
@@ -131,7 +132,7 @@ def gqa_contiguous(batch=8, capacity=131072, num_q_heads=32, num_kv_heads=8, hea
 
 def prefill_append(batch=4, lnew=170, num_heads=32, head_dim=128, old_lo=0, old_hi=512,
                    pool=1000, dtype="f16", seed=1004, device="cpu", dist="uniform",
-                   num_kv_heads=None):
+                   num_kv_heads=None, page_size=PAGE_SIZE):
     """Causal prefill with the new tokens' k/v appended in the same call.
 
     ``old_b ~ U[old_lo, old_hi]`` cached tokens per sequence; ``lnew`` new
@@ -143,12 +144,12 @@ def prefill_append(batch=4, lnew=170, num_heads=32, head_dim=128, old_lo=0, old_
     hkv = num_heads if num_kv_heads is None else num_kv_heads
     cpu_g = torch.Generator().manual_seed(seed)
     old = torch.randint(old_lo, old_hi + 1, (batch,), generator=cpu_g)
-    pages = [-(-(int(o) + lnew) // PAGE_SIZE) for o in old]
-    pool = max(pool, sum(pages))
+    pages = [-(-(int(o) + lnew) // page_size) for o in old]
+    pool = max(pool if page_size == PAGE_SIZE else 0, sum(pages))
     table = _distinct_tables(pages, pool, cpu_g, device)
     g = _gen(seed, device)
-    k_cache = _values((pool, PAGE_SIZE, hkv, head_dim), dt, dist, g, device)
-    v_cache = _values((pool, PAGE_SIZE, hkv, head_dim), dt, dist, g, device)
+    k_cache = _values((pool, page_size, hkv, head_dim), dt, dist, g, device)
+    v_cache = _values((pool, page_size, hkv, head_dim), dt, dist, g, device)
     q = _values((batch, lnew, num_heads, head_dim), dt, dist, g, device)
     k_new = _values((batch, lnew, hkv, head_dim), dt, dist, g, device)
     v_new = _values((batch, lnew, hkv, head_dim), dt, dist, g, device)
@@ -160,7 +161,7 @@ def prefill_append(batch=4, lnew=170, num_heads=32, head_dim=128, old_lo=0, old_
 
 def unified_mixed(num_heads=32, head_dim=128, prefill_lens=(100, 500, 1000), prefix_hi=2048,
                   num_decode=64, ctx_lo=1024, ctx_hi=4096, dtype="bf16", seed=1005,
-                  device="cpu", num_kv_heads=None, pad_to=0):
+                  device="cpu", num_kv_heads=None, pad_to=0, page_size=PAGE_SIZE):
     """One mixed batch: chunked-prefill sequences plus decode sequences.
 
     Prefill sequence j has ``prefill_lens[j]`` query tokens over a cached
@@ -181,15 +182,15 @@ def unified_mixed(num_heads=32, head_dim=128, prefill_lens=(100, 500, 1000), pre
     if pad_to > n_real:
         q_lens += [0] * (pad_to - n_real)
         k_lens += [0] * (pad_to - n_real)
-    pages = [-(-k // PAGE_SIZE) for k in k_lens]
+    pages = [-(-k // page_size) for k in k_lens]
     pool = sum(pages)
     table = _distinct_tables(pages, pool, cpu_g, device)
     cu = [0]
     for l in q_lens:
         cu.append(cu[-1] + l)
     g = _gen(seed, device)
-    k_cache = _values((pool, PAGE_SIZE, hkv, head_dim), dt, "normal", g, device)
-    v_cache = _values((pool, PAGE_SIZE, hkv, head_dim), dt, "normal", g, device)
+    k_cache = _values((pool, page_size, hkv, head_dim), dt, "normal", g, device)
+    v_cache = _values((pool, page_size, hkv, head_dim), dt, "normal", g, device)
     q = _values((cu[-1], num_heads, head_dim), dt, "normal", g, device)
     return dict(q=q, k_cache=k_cache, v_cache=v_cache,
                 cu_seqlens_q=torch.tensor(cu, dtype=torch.int32, device=device),

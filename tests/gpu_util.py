@@ -34,7 +34,7 @@ def oracle_kvcache(w, causal=None, rows=None):
         old = int(w["cache_seqlens"][b])
         lk = old + lnew
         if table is not None:
-            npg = -(-old // 16)
+            npg = -(-old // w["k_cache"].shape[1])
             pages = table[b, :npg].long()
             kc = np64(w["k_cache"][pages])
             vc = np64(w["v_cache"][pages])
@@ -79,7 +79,7 @@ def oracle_varlen(w, seqs=None):
         q0, q1 = cu[b], cu[b + 1]
         if q1 == q0:
             continue
-        npg = -(-lens[b] // 16)
+        npg = -(-lens[b] // w["k_cache"].shape[1])
         pages = table[b, :npg].long()
         kc = np64(w["k_cache"][pages])
         vc = np64(w["v_cache"][pages])

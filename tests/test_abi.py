@@ -53,14 +53,16 @@ def _t4(stride_b=16 * 2 * 64, stride_t=2 * 64, stride_h=64, ptr=4096):
 
 def _kvcache_call(lib, **kw):
     args = dict(q=4096, q_sb=256, q_st=256, q_sh=64, k=_t4(), v=_t4(), k_new=None, v_new=None,
-                lnew=0, seqlens=4096, table=4096, bt_stride=4, max_pages=4, B=2, Lq=1, Hq=4,
+                lnew=0, seqlens=4096, table=4096, bt_stride=4, max_pages=4, page_size=16, B=2,
+                Lq=1, Hq=4,
                 Hkv=2, D=64, extent=8, max_k=64, scale=0.125, causal=0, splits=0, out=4096,
                 lse=None, ws=None, ws_bytes=0, err=None, dtype=pa.PA_F16)
     args.update(kw)
     a = args
     return lib.pa_fwd_kvcache(a["q"], a["q_sb"], a["q_st"], a["q_sh"], a["k"], a["v"],
                               a["k_new"], a["v_new"], a["lnew"], a["seqlens"], a["table"],
-                              a["bt_stride"], a["max_pages"], a["B"], a["Lq"], a["Hq"], a["Hkv"],
+                              a["bt_stride"], a["max_pages"], a["page_size"], a["B"], a["Lq"],
+                              a["Hq"], a["Hkv"],
                               a["D"], a["extent"], a["max_k"], a["scale"], a["causal"],
                               a["splits"], a["out"], a["lse"], a["ws"], a["ws_bytes"], a["err"],
                               a["dtype"], None)
@@ -79,6 +81,8 @@ def test_validation_rejects_before_any_cuda_call(lib):
     assert _kvcache_call(lib, max_pages=0) == pa.PA_ERR_INVALID_ARG
     assert _kvcache_call(lib, bt_stride=2) == pa.PA_ERR_INVALID_ARG
     assert _kvcache_call(lib, scale=float("nan")) == pa.PA_ERR_INVALID_ARG
+    for bad_page in (0, 8, 24, 48, 512):  # 16 << s, s in [0, 4], only
+        assert _kvcache_call(lib, page_size=bad_page) == pa.PA_ERR_UNSUPPORTED
     assert _kvcache_call(lib, q_sh=7) == pa.PA_ERR_INVALID_ARG
     # a split plan that needs workspace but gets none
     assert _kvcache_call(lib, max_k=4096, table=4096, max_pages=256, bt_stride=256,

@@ -56,7 +56,7 @@ def run_case(w, rotary_dim, interleaved, causal, n_pos=None):
     table = w["block_table"]
     for b in range(w["q"].shape[0]):
         old = lens[b]
-        npg = -(-(old + lnew) // 16)
+        npg = -(-(old + lnew) // w["k_cache"].shape[1])
         pages = table[b, :npg].long()
         # the cache now holds the rotated new keys: within one unit in the last
         # place of the oracle's once-rounded rotation

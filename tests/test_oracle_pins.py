@@ -228,23 +228,26 @@ def test_empty_rows():
     assert np.array_equal(out[2, 0], k[0, 0])
 
 
-def test_page_permutation_matches_contiguous():
+@pytest.mark.parametrize("page", [16, 32, 256])
+def test_page_permutation_matches_contiguous(page):
+    """Any page size: the rows scattered over permuted pages of P slots (the
+    cache's second dimension) give the contiguous result."""
     rng = np.random.default_rng(4)
-    bsz, lk, hkv, hq, d = 3, 70, 2, 4, 8
+    bsz, lk, hkv, hq, d = 3, 70 if page < 256 else 600, 2, 4, 8
     contig_k = rng.standard_normal((bsz, lk, hkv, d))
     contig_v = rng.standard_normal((bsz, lk, hkv, d))
-    npg = -(-lk // 16)
+    npg = -(-lk // page)
     pool = bsz * npg
     perm = rng.permutation(pool)
     table = perm.reshape(bsz, npg)
-    kc = np.zeros((pool, 16, hkv, d))
-    vc = np.zeros((pool, 16, hkv, d))
+    kc = np.zeros((pool, page, hkv, d))
+    vc = np.zeros((pool, page, hkv, d))
     for b in range(bsz):
         for t in range(lk):
-            kc[table[b, t // 16], t % 16] = contig_k[b, t]
-            vc[table[b, t // 16], t % 16] = contig_v[b, t]
+            kc[table[b, t // page], t % page] = contig_k[b, t]
+            vc[table[b, t // page], t % page] = contig_v[b, t]
     q = rng.standard_normal((bsz, 2, hq, d))
-    lens = [lk, 50, 17]
+    lens = [lk, 50, 17] if page < 256 else [lk, 300, 257]
     o1, l1 = oracle.fwd_kvcache(q, kc, vc, lens, table, causal=True)
     o2, l2 = oracle.fwd_kvcache(q, contig_k, contig_v, lens, None, causal=True)
     np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)

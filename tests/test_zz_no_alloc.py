@@ -45,7 +45,8 @@ def _raw_noalloc(w, out, lse, err, num_splits):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return lib.pa_fwd_kvcache_noalloc(
         p(q), q.stride(0), q.stride(1), q.stride(2), t4(kc), t4(vc), p(kn), p(vn), lnew,
-        p(w["cache_seqlens"]), p(table), bt_stride, max_pages, B, lq, hq, hkv, d, extent, max_k,
+        p(w["cache_seqlens"]), p(table), bt_stride, max_pages, 16, B, lq, hq, hkv, d, extent,
+        max_k,
         float(w["scale"]), int(bool(w["causal"])), num_splits, p(out), p(lse), p(err),
         pa.PA_BF16 if q.dtype == torch.bfloat16 else pa.PA_F16, stream)
 
@@ -106,7 +107,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert need > pa.PA_NOALLOC_SCRATCH_BYTES
     t4 = pa.pa_tensor4(4096, 1 << 20, 1024, 128)
     rc = lib.pa_fwd_kvcache_noalloc(4096, 64 * 128, 64 * 128, 128, t4, t4, None, None, 0, 4096,
-                                    4096, 8192, 8192, 256, 1, 64, 8, 128, 1 << 16, 131072,
+                                    4096, 8192, 8192, 16, 256, 1, 64, 8, 128, 1 << 16, 131072,
                                     1.0 / math.sqrt(128), 0, 128, 4096, None, None, pa.PA_F16,
                                     None)
     assert rc == pa.PA_ERR_WORKSPACE
