@@ -173,6 +173,14 @@ __device__ __forceinline__ int last_le(const int* pre, int n, int x) {
 // round-robin stay in step, and the query tiles of a head stream its K/V
 // through L2 together.  Kind-1 units have one item; their second sub-item (and
 // the second of an odd middle pair) is empty (kind -1, no rows, no tiles).
+// Work units are (item index idx, half u) pairs, wu = 2 idx + u, dealt to the
+// CTAs round-robin by idx.  A kind-0 index carries a pair of query tiles
+// (u = 0 and 1); a packed index only u = 0, so its u = 1 half is skipped from
+// the schedule alone, without looking the unit up (every role skips alike).
+__device__ __forceinline__ bool empty_half(const Sched& sc, int wu) {
+  return (wu & 1) && (sc.uniform ? sc.packed_u : (wu >> 1) >= sc.total0);
+}
+
 __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc, int idx, int u) {
   Item it;
   int b, head, t = 0, s = 0;
@@ -436,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+      if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
       const int g = it.kind == 0 ? it.head / p.G : it.head;
@@ -557,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto kv_par = [](int t) { return (uint32_t)((t / Tr::kStages) & 1); };
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+      if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
       if (is_qk) {
@@ -660,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kDH = D / 2;  // O columns per half
     int tctr = 0, a = 0;
     for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+      if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       const bool valid = r < it.nrows;
       const bool quarter_live = quarter * 32 < it.nrows;  // any valid row in this quarter
