@@ -26,9 +26,12 @@
 //   warps 12-13 idle: they only place the issuers below on the schedulers
 //              (warp % 4) of the V producers, away from the K producers'.
 //   warp 14    TMEM owner and P V issuer: O += P V with P read from TMEM.
-//   warp 15    Q K^T issuer: S into one of three TMEM buffers, tile t once P V
-//              of tile t-3 (whose P occupies the buffer) has completed.
-// TMEM: S/P of tile t in cols [128 (t % 3), +128), O [384, 384+D).
+//   warp 15    Q K^T issuer: copies each item's Q into TMEM (tcgen05.cp), then
+//              S = Q K^T with Q from TMEM and K from shared memory into one of
+//              NB TMEM buffers, tile t once P V of tile t-NB (whose P occupies
+//              the buffer) has completed.
+// TMEM: S/P of tile t in cols [128 (t % NB), +128), then O (D columns), then
+// Q (D / 2 columns); NB = 2 for head dim 128, 3 for 64.
 // Pipeline state (stage and buffer parities) runs on across items.
 #include <type_traits>
 
@@ -43,12 +46,14 @@ namespace {
 constexpr int kBM = 128;                 // tile rows
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kTilePages = kBN / kPage;  // 8
-// S/P buffers in TMEM (128 columns each; O follows them).  Q K^T of tile t
-// reuses the buffer of tile t-3 once P V of that tile has completed, so the
-// chain softmax(t) -> P V(t) -> Q K^T(t+3) -> softmax(t+3) spans three tiles.
-constexpr int kSBufs = 3;
-__device__ __forceinline__ int sbuf(int t) { return t % kSBufs; }
-__device__ __forceinline__ uint32_t sbuf_par(int t) { return (uint32_t)((t / kSBufs) & 1); }
+// S/P buffers in TMEM (128 columns each; O and then Q follow them).  Q K^T of
+// tile t reuses the buffer of tile t - NB once P V of that tile has
+// completed, so the chain softmax(t) -> P V(t) -> Q K^T(t+NB) -> softmax(t+NB)
+// spans NB tiles.  Buffer of tile t: t mod NB; barrier phase parity (t / NB) mod 2.
+template <int NB> __device__ __forceinline__ int sbuf_of(int t) { return t % NB; }
+template <int NB> __device__ __forceinline__ uint32_t sbuf_par_of(int t) {
+  return (uint32_t)((t / NB) & 1);
+}
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
 constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
@@ -65,6 +70,10 @@ struct EngTraits {
   static constexpr int kHalves = D / 64;
   static constexpr int kSlab = 128 * 128;  // one 128-row x 128-byte slab
   static constexpr int kStages = (D == 128) ? 2 : 3;
+  // TMEM: kSBufs S/P buffers of 128 columns, O (D columns), Q (D / 2 columns:
+  // two 16-bit values per column) -- 2 x 128 + 128 + 64 = 448 for head dim
+  // 128, 3 x 128 + 64 + 32 = 480 for 64, of 512.
+  static constexpr int kSBufs = (D == 128) ? 2 : 3;
   static constexpr int kQBytes = kHalves * kSlab;
   static constexpr int kKVBytes = kHalves * kSlab;
   static constexpr int kOffQ = 0;
@@ -73,6 +82,7 @@ struct EngTraits {
   static constexpr int kOffPre = kOffV + kStages * kKVBytes;  // two int[kEngineMaxB + 1] prefix sums
   static constexpr int kOffBar = kOffPre + ((2 * (kEngineMaxB + 1) * 4 + 15) & ~15);
   static constexpr int kNumBars = 2 + 4 * kStages + 3 * kSBufs + 1 + 1;
+  static_assert(kSBufs * 128 + D + D / 2 <= 512, "TMEM columns");
   // With two stages a K stage is free exactly when Q K^T of the tile two back
   // has completed, which s_full of that parity already signals; likewise a V
   // stage and pv_done.  The producers then wait on those, and the MMA thread
@@ -274,6 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v) {
   using Tr = EngTraits<D>;
+  constexpr int kSBufs = Tr::kSBufs;
+  auto sbuf = [](int t) { return sbuf_of<Tr::kSBufs>(t); };
+  auto sbuf_par = [](int t) { return sbuf_par_of<Tr::kSBufs>(t); };
   using E = Elem<T>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -412,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tslot;
   const uint32_t tO = tbase + kSBufs * 128;
+  const uint32_t tQ = tO + D;  // Q of the current item, copied from shared memory
   auto tS = [&](int t) { return tbase + (uint32_t)(sbuf(t) * 128); };
   const int total = sc.total0 + sc.total1;
 
@@ -571,6 +585,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.ntiles == 0) continue;
       if (is_qk) {
         wait(q_full, (uint32_t)(a & 1), 50);
+        // Q into TMEM: Q K^T then reads only K from shared memory.  The copy
+        // runs in order with this thread's MMAs (after the previous item's
+        // last Q K^T, before this item's first), and frees Q's shared memory
+        // for the next item once it has completed.
+        tc::fence_after_sync();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::cp_128x256b(tQ + kk * 8, dQ + (((kk >> 2) * Tr::kSlab + (kk & 3) * 32) >> 4));
+          tc::commit(q_empty);
+        }
+        __syncwarp();
         for (int j = 0; j < it.ntiles; ++j) {
           const int Tq = tctr + j;
           const int s = Tq % Tr::kStages;
@@ -590,11 +616,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = ((kk >> 2) * Tr::kSlab + (kk & 3) * 32) >> 4;
-              tc::mma_f16_ss(tSq, dQ + off, dK + off, id_qk, kk > 0);
+              tc::mma_f16_ts(tSq, tQ + kk * 8, dK + off, id_qk, kk > 0);
             }
             tc::commit(&s_full[sbuf(Tq)]);
             if (!Tr::kSharedEmpty) tc::commit(&k_empty[s]);
-            if (j == it.ntiles - 1) tc::commit(q_empty);  // Q no longer read
           }
           __syncwarp();
         }

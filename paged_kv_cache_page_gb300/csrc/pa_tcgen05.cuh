@@ -90,6 +90,16 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// Copy a 128-row x 256-bit block (16 elements of 16 bits per row) from shared
+// memory, described like an MMA operand (start address, 128-byte swizzle),
+// into TMEM: row m -> lane m, columns [t_addr, t_addr + 8).  Asynchronous,
+// ordered with this thread's later MMAs; eight of them place a K = 128 A
+// operand in TMEM as mma_f16_ts reads it (two 16-bit values per column).
+__device__ __forceinline__ void cp_128x256b(uint32_t t_addr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(t_addr), "l"(s_desc)
+               : "memory");
+}
+
 // Arrive (once) on `bar` when all previously issued tcgen05 ops of this
 // thread have completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {

@@ -165,3 +165,123 @@ extern "C" __attribute__((visibility("default"))) int pa_selftest_tcgen05_transp
   if (dtype == PA_BF16) return run<__nv_bfloat16>(K, Q, V, P, C4, C5, status, st);
   return -4;
 }
+
+// ---------------------------------------------------------------------------
+// Q copied into TMEM by tcgen05.cp: C1 = Q K^T with Q from shared memory and
+// C2 = Q K^T with Q from TMEM (after eight 128x256b copies of the 128-byte-
+// swizzled Q tile, one per 16-element k-step), M = N = K = 128.
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(192, 1)
+    selftest_cpq_kernel(float* __restrict__ C1, float* __restrict__ C2,
+                        const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k, int32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;            // 2 slabs x 128 rows x 128 B
+  uint8_t* sK = smem + 32768;    // 2 slabs x 128 rows x 128 B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 65536);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+  uint64_t* b_full = &bars[0];
+  uint64_t* mma_done = &bars[1];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(b_full, 1);
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(tslot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  if (warp == 4 && lane == 0) {
+    mbar_arrive_expect_tx(b_full, 2 * 32768);
+    for (int h = 0; h < 2; ++h) {
+      uint8_t* dsts[2] = {sQ + h * 16384, sK + h * 16384};
+      const CUtensorMap* maps[2] = {&tm_q, &tm_k};
+      for (int m = 0; m < 2; ++m)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dsts[m])),
+            "l"(reinterpret_cast<uint64_t>(maps[m])), "r"(h * 64), "r"(0), "r"(smem_u32(b_full))
+            : "memory");
+    }
+  }
+  if (warp == 5 && lane == 0) {
+    if (!mbar_wait(b_full, 0)) atomicExch(status, 1);
+    tc::fence_after_sync();
+    const bool bf = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t id = tc::idesc_f16(128, 128, bf, false);
+    const uint64_t dQ = tc::smem_desc(smem_u32(sQ), 16, 1024);
+    const uint64_t dK = tc::smem_desc(smem_u32(sK), 16, 1024);
+    const uint32_t tQ = tbase + 256;  // Q in TMEM: 64 columns (two 16-bit values each)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+      tc::cp_128x256b(tQ + kk * 8, dQ + off);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+      tc::mma_f16_ss(tbase, dQ + off, dK + off, id, kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+      tc::mma_f16_ts(tbase + 128, tQ + kk * 8, dK + off, id, kk > 0);
+    }
+    tc::commit(mma_done);
+  }
+  if (warp < 4) {
+    if (!mbar_wait(mma_done, 0)) atomicExch(status, 2);
+    tc::fence_after_sync();
+    const int row = warp * 32 + lane;
+    const uint32_t lane_addr = tbase + ((uint32_t)(warp * 32) << 16);
+    for (int c = 0; c < 128; c += 32) {
+      float v[32];
+      tc::tmem_ld32(lane_addr + c, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) C1[row * 128 + c + i] = v[i];
+      tc::tmem_ld32(lane_addr + 128 + c, v);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) C2[row * 128 + c + i] = v[i];
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 5) tc::tmem_dealloc(tbase, 512);
+}
+
+template <typename T>
+int run_cpq(const void* Q, const void* K, float* C1, float* C2, int32_t* status, cudaStream_t st) {
+  const int dt = std::is_same<T, __nv_bfloat16>::value ? PA_BF16 : PA_F16;
+  CUtensorMap mq, mk;
+  if (!encode2d(&mq, Q, dt) || !encode2d(&mk, K, dt)) return -1;
+  const int smem = 1024 + 65536 + 256;
+  if (cudaFuncSetAttribute(selftest_cpq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return -2;
+  selftest_cpq_kernel<T><<<1, 192, smem, st>>>(C1, C2, mq, mk, status);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace
+
+// Q, K: 128 x 128 row-major; C1, C2: 128 x 128 fp32 (Q K^T, Q from shared
+// memory and from TMEM after tcgen05.cp).
+extern "C" __attribute__((visibility("default"))) int pa_selftest_tcgen05_cpq(
+    const void* Q, const void* K, float* C1, float* C2, int dtype, int32_t* status,
+    cudaStream_t st) {
+  if (dtype == PA_F16) return run_cpq<__half>(Q, K, C1, C2, status, st);
+  if (dtype == PA_BF16) return run_cpq<__nv_bfloat16>(Q, K, C1, C2, status, st);
+  return -4;
+}

@@ -69,3 +69,28 @@ def test_tcgen05_transposed_decode_shapes(dtype):
     assert rc == 0 and status.item() == 0
     torch.testing.assert_close(C4, K.float() @ Q[:16].float().T, rtol=1e-4, atol=1e-3)
     torch.testing.assert_close(C5, V.float().T @ P.float().T, rtol=1e-4, atol=1e-3)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_tcgen05_cp_places_an_a_operand_in_tmem(dtype):
+    """tcgen05.cp of the 128-byte-swizzled Q tile (eight 128x256b blocks, one
+    per k-step) into TMEM gives the A operand the TMEM-A MMA reads: Q K^T with
+    Q from TMEM equals Q K^T with Q from shared memory and the reference."""
+    pabuild.build()
+    lib = ctypes.CDLL(pabuild.lib_path(pabuild.SELFTEST_LIB))
+    g = torch.Generator(device=DEV).manual_seed(11)
+    Q = torch.randn((128, 128), generator=g, device=DEV).to(dtype)
+    K = torch.randn((128, 128), generator=g, device=DEV).to(dtype)
+    C1 = torch.full((128, 128), float("nan"), device=DEV)
+    C2 = torch.full((128, 128), float("nan"), device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    rc = lib.pa_selftest_tcgen05_cpq(p(Q), p(K), p(C1), p(C2),
+                                     pa.PA_BF16 if dtype == torch.bfloat16 else pa.PA_F16,
+                                     p(status),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert rc == 0 and status.item() == 0
+    ref = Q.float() @ K.float().T
+    torch.testing.assert_close(C1, ref, rtol=1e-4, atol=1e-3)
+    torch.testing.assert_close(C2, ref, rtol=1e-4, atol=1e-3)
