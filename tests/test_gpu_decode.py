@@ -139,14 +139,20 @@ def test_empty_and_single_key_sequences():
     assert_close(out, lse, ref_o, ref_l, "f16")
 
 
-def test_split_combine_entry_point():
-    g = torch.Generator().manual_seed(16)
-    S, B, Lq, Hq, D = 5, 3, 2, 4, 128
+@pytest.mark.parametrize("S,D", [(5, 128), (32, 128), (32, 64), (45, 128), (70, 64)])
+def test_split_combine_entry_point(S, D):
+    """Up to 32 splits take the lane-per-split path, more take the serial one;
+    both skip empty splits (LSE -inf) without reading their partials."""
+    g = torch.Generator().manual_seed(16 + S)
+    B, Lq, Hq = 4, 2, 4
     o = torch.randn((S, B, Lq, Hq, D), generator=g).float()
     l = torch.randn((S, B, Lq, Hq), generator=g).float() * 3
     l[2, 1] = float("-inf")  # an empty split
     o[2, 1] = float("nan")   # whose partial must not be read
-    nsp = torch.tensor([5, 3, 0], dtype=torch.int32)
+    l[S - 1, 0] = float("-inf")
+    o[S - 1, 0] = float("nan")
+    l[:, 3, 1] = float("-inf")  # a query row with no keys at all
+    nsp = torch.tensor([S, 3, 0, S], dtype=torch.int32)
     out = torch.full((B, Lq, Hq, D), 7.0, dtype=torch.float16, device=DEV)
     lse = torch.full((B, Hq, Lq), 7.0, dtype=torch.float32, device=DEV)
     pa.pa_split_combine(o.to(DEV), l.to(DEV), out, lse, nsp.to(DEV))
@@ -157,8 +163,11 @@ def test_split_combine_entry_point():
             assert torch.all(out[b] == 7.0) and torch.all(lse[b] == 7.0)
             continue
         ref_o, ref_l = oracle.combine_splits(o[:n, b].double().numpy(), l[:n, b].double().numpy())
-        assert np.abs(np64(out[b]) - ref_o).max() <= OUT_TOL["f16"]
-        assert np.abs(np64(lse[b]).transpose(1, 0) - ref_l).max() <= LSE_TOL
+        got_o, got_l = np64(out[b]), np64(lse[b]).transpose(1, 0)
+        empty = np.isneginf(ref_l)
+        assert np.all(got_o[empty] == 0) and np.all(np.isneginf(got_l[empty]))
+        assert np.abs(got_o[~empty] - ref_o[~empty]).max() <= OUT_TOL["f16"]
+        assert np.abs(got_l[~empty] - ref_l[~empty]).max() <= LSE_TOL
 
 
 def test_out_of_range_pages_report_and_do_not_fault():
