@@ -262,7 +262,7 @@ def secondary_measurements(dev, only=None):
             "us": round(us, 1), "tflops": round(fl / us / 1e6, 1),
             "roofline": {"bound": "tensor", "achieved": round(fl / us / 1e6, 1), "peak": tpeak,
                          "unit": "TFLOP/s", "frac": round(fl / us / 1e6 / tpeak, 4),
-                         "peak_source": tsrc, "kernel": "engine_kernel<128, __half>"},
+                         "peak_source": tsrc, "kernel": "prefill_kernel<128, __half>"},
             "flops": fl, "us_with_append": round(us_append, 1),
             "note": "fp16, 32 heads x D 128, causal, keys read through 16-token pages"}
         if only == "prefill":

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libpagedattn.so"
 SOURCES = ["api.cu", "append.cu", "decode.cu", "combine.cu", "noalloc.cu", "engine.cu",
-           "rotary.cu"]
+           "rotary.cu", "prefill.cu"]
 # Encoding self-test of the tensor-core operand layouts: test infrastructure,
 # kept out of the product library.
 SELFTEST_LIB = "libpa_selftest.so"

@@ -453,8 +453,12 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     ep.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
     ep.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
     ep.err = err_word;
-    cudaError_t e = launch_engine(ep, tq1, tq2, tk, tv, D, dtype, grid, st);
-    if (e != cudaSuccess) return cuda_fail(e, "engine launch");
+    // query blocks longer than one packed tile: two 128-row query tiles per
+    // CTA sharing every K/V tile; packed blocks (decode, multi-query decode):
+    // the engine, split over the keys
+    cudaError_t e = pack ? launch_engine(ep, tq1, tq2, tk, tv, D, dtype, grid, st)
+                         : launch_prefill(ep, tq1, tk, tv, D, dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, pack ? "engine launch" : "prefill launch");
     if (s_max > 1) {
       CombineParams c{};
       c.o_part = ep.o_part;

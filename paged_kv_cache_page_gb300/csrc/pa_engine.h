@@ -44,4 +44,12 @@ cudaError_t launch_engine(const EngineParams& p, const CUtensorMap& tm_q1,
                           const CUtensorMap& tm_v, int D, int dtype, int grid, cudaStream_t st);
 int engine_grid();
 
+// Prefill of a kvcache call whose query blocks are longer than one packed tile
+// (uniform query length Lq, cu_seqlens_q == null): two 128-row query tiles of
+// one head per CTA sharing every K/V tile.  Uses p.out, p.lse, the sequence
+// and cache fields, scale_log2 and causal; the split fields are ignored.
+// tm_q: q map with box {64, 1, 128, 1}; tm_k/tm_v as for launch_engine.
+cudaError_t launch_prefill(const EngineParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, int D, int dtype, cudaStream_t st);
+
 }  // namespace pa

@@ -113,7 +113,9 @@ def test_page_placement_is_bit_invariant():
 
 
 def test_contiguous_gqa_split_kv_cache():
-    w = wl.gqa_contiguous(capacity=16384, device=DEV)
+    """B8, 32 q / 8 kv heads, D 128, bf16, lengths U[1024, 8192] in a
+    131072-token contiguous cache: the launch the benchmark times, every row."""
+    w = wl.gqa_contiguous(device=DEV)
     B, cap = 8, w["capacity"]
     hkv, d = w["num_kv_heads"], w["head_dim"]
     kc = torch.zeros((B, cap, hkv, d), dtype=torch.bfloat16, device=DEV)
