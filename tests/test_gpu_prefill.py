@@ -120,3 +120,42 @@ def test_long_causal_prefill_sampled():
     out, lse = run(w)
     for (b, h), (ro, rl) in ref.items():
         assert_close(out[b:b + 1, :, h:h + 1], lse[b:b + 1, h:h + 1], ro, rl, "bf16")
+
+
+@pytest.mark.parametrize("lnew,d,hq,hkv,causal,dtype", [
+    (600, 128, 8, 1, True, "bf16"),   # 5 query tiles: pairs 2 + 0 (tile 5 past the queries), pair 1 alone
+    (768, 64, 16, 2, True, "f16"),    # 6 full query tiles
+    (1025, 128, 4, 4, False, "f16"),  # 9 query tiles, the last holding one row; all keys visible
+])
+def test_prefill_query_tile_pairs(lnew, d, hq, hkv, causal, dtype):
+    """Query blocks of several 128-row tiles, run two tiles of one head per
+    CTA: a unit's heavier and lighter pair, an odd middle pair, a pair whose
+    second tile lies past the queries, GQA up to 8 query heads per kv head,
+    over cached prefixes of different lengths."""
+    w = wl.prefill_append(batch=2, lnew=lnew, num_heads=hq, num_kv_heads=hkv, head_dim=d,
+                          old_lo=0, old_hi=600, dtype=dtype, dist="normal", seed=50 + lnew,
+                          device=DEV)
+    w["causal"] = causal
+    ref_o, ref_l = oracle_kvcache(w)
+    out, lse = run(w)
+    assert_close(out, lse, ref_o, ref_l, dtype)
+
+
+def test_prefill_lengths_beyond_table_report():
+    """A sequence whose length exceeds its block table: the call reports
+    PA_DEVERR_LENGTH for it and writes O = 0, LSE = -inf for its rows; the
+    other sequence is unaffected."""
+    w = wl.prefill_append(batch=2, lnew=200, num_heads=4, head_dim=64, old_lo=50, old_hi=300,
+                          dtype="f16", dist="normal", seed=47, device=DEV)
+    lens = w["cache_seqlens"] + 200  # the new tokens taken as already cached
+    w.update(k_new=None, v_new=None, cache_seqlens=lens)
+    width = w["block_table"].shape[1]
+    w["cache_seqlens"][0] = width * 16 + 1
+    err = pa.new_err_word(DEV)
+    out, lse = pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],
+                                 w["block_table"], scale=w["scale"], causal=True, err=err)
+    torch.cuda.synchronize()
+    assert err[0].item() == pa.PA_DEVERR_LENGTH and err[1].item() == 0, err.tolist()
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    ref_o, ref_l = oracle_kvcache(w, rows=[1])
+    assert_close(out[1:], lse[1:], ref_o, ref_l, "f16")
