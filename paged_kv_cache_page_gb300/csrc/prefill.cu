@@ -42,6 +42,7 @@ constexpr int kPTileBoxes = kPN / kPage;  // 16-token boxes per KV tile (8)
 constexpr int kPWarpK = 8, kPWarpV = 9, kPWarpPV = 10, kPWarpQK = 11;
 constexpr int kPThreads = 12 * 32;
 constexpr float kPRescaleThreshold = 8.0f;
+
 template <int D>
 struct PfTraits {
   static constexpr int kHalves = D / 64;         // 64-column (128-byte) slabs per row
