@@ -488,6 +488,31 @@ def dist_env():
     return rank, world, local
 
 
+def replica_seed(rank):
+    """Seed of a rank's batch: every rank is an independent replica with its
+    own sequences (weak scaling; no data crosses ranks)."""
+    return 1002 + rank
+
+
+def max_over_ranks(x, world, device=None):
+    """The largest `x` over all ranks (the slowest rank's time), `x` itself on
+    one rank; on whatever backend the process group was created with."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes, steps, world, elapsed_ms):
+    """Whole-job throughput in GB/s: the bytes all ranks processed over the
+    slowest rank's time."""
+    return step_bytes * steps * world / (elapsed_ms * 1e-3) / 1e9
+
+
 def cpu_oracle_rate(w_cpu, seqs, lnew):
     """Time the CPU oracle on sequences `seqs` of the workload; returns
     (GB/s-equivalent, seconds, sample description)."""
@@ -650,7 +675,7 @@ def main():
     hq, hkv, d = WORKLOAD["num_q_heads"], WORKLOAD["num_kv_heads"], WORKLOAD["head_dim"]
     # each rank is an independent replica with its own sequences (weak scaling)
     w = wl.paged_decode(B, ctx, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, lnew=lnew,
-                        seed=1002 + rank, device=dev)
+                        seed=replica_seed(rank), device=dev)
     out = torch.empty((B, lnew, hq, d), dtype=torch.float16, device=dev)
     lse = torch.empty((B, hq, lnew), dtype=torch.float32, device=dev)
     ws_bytes = pa.fwd_kvcache_workspace_size(B, lnew, hq, hkv, d, ctx, 0)
@@ -686,12 +711,9 @@ def main():
         barrier()
     elapsed_ms = t_all0.elapsed_time(t_all1)
     per_launch_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     step_bytes = algorithmic_bytes(B, ctx, lnew, lnew, hq, hkv, d)
-    value = step_bytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, args.steps, world, elapsed_ms)
 
     # end-to-end through the public API with host buffers: inputs of the step
     # (q, new k/v, lengths, block table) copied from pinned host memory, output
@@ -730,11 +752,8 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e_value = whole_job_gbs(step_bytes, args.steps, world, e2e_ms)
 
     if rank == 0:
         peak, peak_src = read_peaks()
