@@ -280,6 +280,23 @@ def secondary_measurements(dev, only=None):
         res["prefill_append_4x170"] = {"us": round(us, 1), "tflops": round(fl / us / 1e6, 2),
                                        "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4),
                                        "l2": "flushed between calls"}
+    if only in (None, "gqa"):
+        gqa_leg(dev, stream, only, hpeak, res)
+        if only == "gqa":
+            return res
+    unified_leg(dev, stream, only, hpeak, tpeak, res)
+    if only == "unified":
+        return res
+    rest_legs(dev, stream, hpeak, res)
+    return res
+
+
+def gqa_leg(dev, stream, only, hpeak, res):
+    import torch
+
+    import paged_kv_cache_page_gb300 as pa
+    from paged_kv_cache_page_gb300 import workloads as wl
+
     # GQA split-KV decode on a contiguous 131072-token cache, lengths U[1024, 8192]
     w = wl.gqa_contiguous(device=dev)
     kc = torch.empty((8, w["capacity"], 8, 128), dtype=torch.bfloat16, device=dev)
@@ -305,8 +322,14 @@ def secondary_measurements(dev, only=None):
                                       "l2": "flushed between calls",
                                       "us_l2_warm": None if us_warm is None else round(us_warm, 1)}
     del kc, vc
-    if only == "gqa":
-        return res
+
+
+def unified_leg(dev, stream, only, hpeak, tpeak, res):
+    import torch
+
+    import paged_kv_cache_page_gb300 as pa
+    from paged_kv_cache_page_gb300 import workloads as wl
+
     # unified mixed batch in one launch: prefills of 100/500/1000 query tokens
     # over cached prefixes U[0, 2048] + 64 decodes with contexts U[1024, 4096],
     # 32 heads x D 128, bf16, causal
@@ -319,7 +342,7 @@ def secondary_measurements(dev, only=None):
                                           w["cu_seqlens_q"], w["seqlens_k"], w["block_table"],
                                           w["max_seqlen_q"], w["max_seqlen_k"], out=out,
                                           workspace=ws, return_lse=False)
-    us = time_calls(fn, 20, 5, stream)
+    us = time_calls(fn, 20 if only is None else 3, 5 if only is None else 3, stream)
     cu = w["cu_seqlens_q"].cpu().tolist()
     kl = w["seqlens_k"].cpu().tolist()
     ql = [cu[i + 1] - cu[i] for i in range(len(kl))]
@@ -330,6 +353,14 @@ def secondary_measurements(dev, only=None):
                                    "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4),
                                    "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4)}
     del w, out, ws
+
+
+def rest_legs(dev, stream, hpeak, res):
+    import torch
+
+    import paged_kv_cache_page_gb300 as pa
+    from paged_kv_cache_page_gb300 import workloads as wl
+
     # multi-query (speculative) decode: 6 new tokens per sequence appended in the
     # call, causal among themselves, 64 sequences x ctx 4096, GQA 32/8, D 128, bf16
     w = wl.paged_decode(batch=64, ctx=4096, num_q_heads=32, num_kv_heads=8, head_dim=128,
@@ -634,7 +665,7 @@ def main():
                          "N=128 with A in TMEM) next to N=256; one JSON line each")
     ap.add_argument("--sweep", action="store_true",
                     help="time the paged decode sweep (ctx 512..4096 x batch 1..256) instead")
-    ap.add_argument("--only", choices=["prefill", "gqa"],
+    ap.add_argument("--only", choices=["prefill", "gqa", "unified"],
                     help="time only this secondary leg (for profiling runs)")
     args = ap.parse_args()
     WORKLOAD["batch"], WORKLOAD["ctx"] = args.batch, args.ctx
