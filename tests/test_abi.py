@@ -47,6 +47,40 @@ def test_binding_signatures_cover_header(lib):
     assert set(declared_symbols()) == set(pa._SIGNATURES)
 
 
+def declared_prototypes():
+    """name -> list of parameter declarations, from the header's PA_API
+    prototypes (comments removed)."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    out = {}
+    for m in re.finditer(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [x.strip() for x in m.group(2).split(",") if x.strip()]
+        out[m.group(1)] = [] if params == ["void"] else params
+    return out
+
+
+def test_binding_argument_counts_and_kinds_match_header(lib):
+    """Every binding signature has the header's parameter count, with each
+    pointer / 64-bit / 32-bit / float / struct parameter marshalled as one."""
+    protos = declared_prototypes()
+    assert set(protos) == set(pa._SIGNATURES)
+    for name, params in protos.items():
+        argtypes = pa._SIGNATURES[name][1]
+        assert len(argtypes) == len(params), (name, len(argtypes), len(params))
+        for decl, at in zip(params, argtypes):
+            if "*" in decl or decl.startswith("pa_stream_t"):
+                assert at in (ctypes.c_void_p, ctypes.c_char_p), (name, decl, at)
+            elif decl.startswith("pa_tensor4"):
+                assert at is pa.pa_tensor4, (name, decl, at)
+            elif decl.split()[0] in ("int64_t", "size_t"):
+                assert ctypes.sizeof(at) == 8, (name, decl, at)
+            elif decl.split()[0] == "float":
+                assert at is ctypes.c_float, (name, decl, at)
+            else:
+                assert decl.split()[0] in ("int", "int32_t") and ctypes.sizeof(at) == 4, (name, decl, at)
+
+
 def _t4(stride_b=16 * 2 * 64, stride_t=2 * 64, stride_h=64, ptr=4096):
     return pa.pa_tensor4(ptr, stride_b, stride_t, stride_h)
 
