@@ -53,9 +53,10 @@ bool mult8(int64_t s) { return s > 0 && (s % 8) == 0; }
 constexpr int kSplitCapTargetCtas = 304;  // 152 SMs x 2 resident decode CTAs
 constexpr int kMinChunkPages = 8;         // each split streams >= 128 keys
 constexpr int kMaxSplits = 128;
-// Query blocks of at most this many rows per kv head run on the CUDA-core
-// split-KV decode kernel; larger ones on the tensor-core engine.
-constexpr int kCudaCoreRows = 2;
+// Query blocks of at most this many rows per kv head run on the split-KV
+// decode kernel (1-2 rows: CUDA-core consumers; 3-16: warp-level tensor-core
+// consumer); larger ones on the tcgen05 engine.
+constexpr int kCudaCoreRows = 16;
 
 int plan_s_max(int B, int Hkv, int max_seqlen_k, int num_splits) {
   const int max_pages = std::max(1, (max_seqlen_k + kPage - 1) / kPage);
@@ -136,7 +137,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 int decode_resident_ctas(int D, int dtype, int rmax) {
   static int cache[2][2][4] = {};
-  const int di = D == 128 ? 1 : 0, ri = rmax == 1 ? 0 : rmax == 2 ? 1 : rmax == 4 ? 2 : 3;
+  const int di = D == 128 ? 1 : 0, ri = rmax == 1 ? 0 : rmax == 2 ? 1 : rmax == 8 ? 2 : 3;
   int& c = cache[di][dtype][ri];
   if (c == 0) {
     const int per_sm = std::max(1, decode_ctas_per_sm(D, dtype, rmax));
@@ -164,7 +165,7 @@ int check_common(int dtype, int D, int Hq, int Hkv) {
 }
 
 int rows_template(int rows) {
-  return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : 8;
+  return rows <= 1 ? 1 : rows <= 2 ? 2 : rows <= 8 ? 8 : 16;
 }
 
 }  // namespace
@@ -493,10 +494,13 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   const bool paged = block_table != nullptr;
   const int64_t dim2 = paged ? page_rows : cache_extent;
   const int64_t dim3 = paged ? cache_extent : B;
+  // 1-2 rows: full-row unswizzled page boxes; more: 64-column boxes with the
+  // 128-byte swizzle that the tensor-core consumer's ldmatrix reads
+  const bool swz = rmax > 2;
   if (!encode_cache_map(&tmk, k_cache.ptr, dtype, D, Hkv, dim2, dim3, k_cache.stride_h,
-                        k_cache.stride_t, k_cache.stride_b, D, kPage, false) ||
+                        k_cache.stride_t, k_cache.stride_b, swz ? 64 : D, kPage, swz) ||
       !encode_cache_map(&tmv, v_cache.ptr, dtype, D, Hkv, dim2, dim3, v_cache.stride_h,
-                        v_cache.stride_t, v_cache.stride_b, D, kPage, false))
+                        v_cache.stride_t, v_cache.stride_b, swz ? 64 : D, kPage, swz))
     return fail(PA_ERR_INVALID_ARG, "cannot encode a TMA descriptor for the cache views");
 
   DecodeParams p{};

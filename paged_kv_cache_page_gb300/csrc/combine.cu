@@ -44,10 +44,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     }
     const int n = p.nsplit ? min(__ldg(p.nsplit + b), p.S) : p.S;
     if (n <= 0) continue;
-    // max of the split LSEs (natural log) -> log2 domain
+    // max of the split LSEs (natural log) -> log2 domain; lane s keeps the
+    // LSE of split s (and of s + 32, ...)
     float M = neg_inf();
-    for (int s = lane; s < n; s += 32)
-      M = fmaxf(M, __ldg(p.lse_part + ((long long)s * NR + row) * p.Hq + h) * kLog2e);
+    float my_ls = neg_inf();
+    for (int s = lane; s < n; s += 32) {
+      const float ls = __ldg(p.lse_part + ((long long)s * NR + row) * p.Hq + h) * kLog2e;
+      if (s == lane) my_ls = ls;
+      M = fmaxf(M, ls);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[kPVE];
@@ -55,23 +60,41 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     for (int e = 0; e < kPVE; ++e) acc[e] = 0.f;
     float L = 0.f;
     if (M != neg_inf()) {
-      for (int s = 0; s < n; ++s) {
-        const long long idx = ((long long)s * NR + row) * p.Hq + h;
-        const float ls = __ldg(p.lse_part + idx) * kLog2e;
-        if (ls == neg_inf()) continue;  // empty split: its O_s is not read
-        const float wgt = ex2(ls - M);
-        L += wgt;
-        const float* op = p.o_part + idx * D + lane * kPVE;
-        if constexpr (kPVE == 4) {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(op));
-          acc[0] = fmaf(wgt, v.x, acc[0]);
-          acc[1] = fmaf(wgt, v.y, acc[1]);
-          acc[2] = fmaf(wgt, v.z, acc[2]);
-          acc[3] = fmaf(wgt, v.w, acc[3]);
-        } else {
-          const float2 v = __ldg(reinterpret_cast<const float2*>(op));
-          acc[0] = fmaf(wgt, v.x, acc[0]);
-          acc[1] = fmaf(wgt, v.y, acc[1]);
+      // four splits per step: their partial rows are loaded together; an
+      // empty split (LSE -inf) gets weight 0 and its partial is not read
+      constexpr int kU = 4;
+      for (int s0 = 0; s0 < n; s0 += kU) {
+        float wgt[kU];
+        float v[kU][kPVE];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int s = s0 + u;
+          float ls = neg_inf();
+          if (s < 32) {
+            ls = __shfl_sync(0xffffffffu, my_ls, s & 31);
+          } else if (s < n) {
+            ls = __ldg(p.lse_part + ((long long)s * NR + row) * p.Hq + h) * kLog2e;
+          }
+          const bool live = s < n && ls != neg_inf();
+          wgt[u] = live ? ex2(ls - M) : 0.f;
+          const float* op = p.o_part + (((long long)s * NR + row) * p.Hq + h) * D + lane * kPVE;
+#pragma unroll
+          for (int e = 0; e < kPVE; ++e) v[u][e] = 0.f;
+          if (live) {
+            if constexpr (kPVE == 4) {
+              const float4 x = __ldg(reinterpret_cast<const float4*>(op));
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+              const float2 x = __ldg(reinterpret_cast<const float2*>(op));
+              v[u][0] = x.x; v[u][1] = x.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          L += wgt[u];
+#pragma unroll
+          for (int e = 0; e < kPVE; ++e) acc[e] = fmaf(wgt[u], v[u][e], acc[e]);
         }
       }
     }

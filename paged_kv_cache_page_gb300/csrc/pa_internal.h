@@ -98,13 +98,14 @@ cudaError_t launch_rotary(const RotaryParams& p, int dtype, cudaStream_t st);
 // wait on the device until it has completed and its writes are visible).
 cudaError_t launch_combine(const CombineParams& p, int D, int dtype, int rows_total,
                            cudaStream_t st, bool dependent = false);
-// Decode: `rmax` in {1,2,4,8}.  tmk/tmv are 4-D tensor maps of the caches
-// with box {D, 1, 16, 1}.
+// Decode: `rmax` in {1, 2, 8, 16} (rows per kv head, rounded up).  tmk/tmv
+// are 4-D tensor maps of the caches with box {D, 1, 16, 1} unswizzled (rmax
+// 1, 2) or {64, 1, 16, 1} with the 128-byte swizzle (rmax 8, 16).
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           int D, int dtype, int rmax, cudaStream_t st);
 // Resident CTAs per SM of the decode kernel for this configuration (0 on error).
 int decode_ctas_per_sm(int D, int dtype, int rmax);
-constexpr int kDecodeMaxRows = 8;
+constexpr int kDecodeMaxRows = 16;
 constexpr int kDecodeMaxSchedB = 512;
 
 // Host helpers (api.cu).

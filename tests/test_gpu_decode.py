@@ -1,4 +1,4 @@
-"""GPU parity of the split-KV decode path (pa_fwd_kvcache with Lq*G <= 8)
+"""GPU parity of the split-KV decode path (pa_fwd_kvcache with Lq*G <= 16)
 against the CPU oracle, plus the standalone combine and the device-side error
 word.  Calls go through the C ABI (ctypes binding)."""
 
@@ -209,3 +209,26 @@ def test_full_size_decode_sweep_point_sampled():
     ref_o, ref_l = oracle_kvcache(w, rows=rows)
     out, lse = run(w)
     assert_close(out, lse, ref_o, ref_l, "f16", rows=rows)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("hq,hkv,lq,splits", [(32, 8, 1, 0), (64, 8, 1, 0), (16, 4, 2, 3),
+                                              (12, 4, 1, 5), (8, 1, 1, 0), (6, 2, 2, 0)])
+def test_gqa_rows_share_each_key(dtype, d, hq, hkv, lq, splits):
+    """3-8 query rows per kv head (GQA decode, short multi-query decode with a
+    causal in-call append): the CUDA-core decode layout that reduce-scatters
+    the rows' dot products, including padded row counts (3 and 6 of 4 and 8),
+    ragged lengths whose last page is partial, and forced split counts."""
+    lens = [1000, 37, 700, 16, 2, 513]
+    w = wl.paged_decode(len(lens), 0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, lens=lens,
+                        lnew=lq, seed=31 + hq + lq + d, device=DEV, dtype=dtype)
+    w["causal"] = lq > 1
+    ref_o, ref_l = oracle_kvcache(w)
+    kc0 = w["k_cache"].clone()
+    out, lse = run(w, num_splits=splits)
+    assert_close(out, lse, ref_o, ref_l, dtype)
+    kn, table = bits(w["k_new"]), w["block_table"].cpu().numpy()
+    expect, _ = oracle.append_kv(bits(kc0), bits(kc0), kn, kn, w["cache_seqlens"].cpu().numpy(),
+                                 table)
+    assert np.array_equal(bits(w["k_cache"]), expect)
