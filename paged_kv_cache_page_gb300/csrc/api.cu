@@ -111,11 +111,14 @@ struct SplitWorkspace {
   size_t off_nsplit, off_lse, off_o, total;
 };
 
-SplitWorkspace split_workspace_layout(int B, long long rows, int Hq, int D, int s_max) {
+// Split workspace: split counts [B, Hkv] (int32), then LSE partials
+// [s_max, rows, Hq] and O partials [s_max, rows, Hq, D] (fp32), each
+// 256-byte aligned.
+SplitWorkspace split_workspace_layout(int B, int Hkv, long long rows, int Hq, int D, int s_max) {
   SplitWorkspace w{};
   if (s_max <= 1) return w;
   w.off_nsplit = 0;
-  w.off_lse = align256((size_t)B * 4);
+  w.off_lse = align256((size_t)B * Hkv * 4);
   w.off_o = w.off_lse + align256((size_t)s_max * rows * Hq * 4);
   w.total = w.off_o + align256((size_t)s_max * rows * Hq * D * 4);
   return w;
@@ -280,7 +283,7 @@ PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int 
   // 128-row tiles of one head are never split
   if (rows > kEngineMaxRows || (rows > kCudaCoreRows && kEngineMaxRows % G != 0)) return 0;
   const int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
-  return split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max).total;
+  return split_workspace_layout(B, Hkv, (long long)B * Lq, Hq, D, s_max).total;
 }
 
 // scratch for the rotated q and k_new, ahead of pa_fwd_kvcache's own workspace
@@ -358,7 +361,7 @@ PA_API size_t pa_fwd_varlen_workspace_size(int B, int total_q, int max_seqlen_q,
   if (B <= 0 || total_q <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return 0;
   (void)max_seqlen_q;
   const int s_max = plan_s_max(std::min(B, kDecodeMaxSchedB), Hkv, max_seqlen_k, 0);
-  return split_workspace_layout(B, total_q, Hq, D, s_max).total;
+  return split_workspace_layout(B, Hkv, total_q, Hq, D, s_max).total;
 }
 
 PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
@@ -416,7 +419,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     }
     const bool pack = rows <= kEngineMaxRows && (kEngineMaxRows % G) == 0;
     const int s_max = pack ? plan_s_max(B, Hkv, max_seqlen_k, num_splits) : 1;
-    const SplitWorkspace ws = split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max);
+    const SplitWorkspace ws = split_workspace_layout(B, Hkv, (long long)B * Lq, Hq, D, s_max);
     if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
       return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
                   workspace_bytes);
@@ -469,6 +472,8 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
       c.o_part = ep.o_part;
       c.lse_part = ep.lse_part;
       c.nsplit = ep.nsplit;
+      c.ns_stride = 1;
+      c.ns_group = Hq;
       c.S = s_max;
       c.B = B; c.Lq = Lq; c.Hq = Hq;
       c.cu_seqlens_q = nullptr;
@@ -485,7 +490,7 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   const int resident = decode_resident_ctas(D, dtype, rmax);
   int s_max = plan_s_max(B, Hkv, max_seqlen_k, num_splits);
   if (num_splits == 0 && !decode_splits_useful(B, Hkv, max_seqlen_k, s_max, resident)) s_max = 1;
-  const SplitWorkspace ws = split_workspace_layout(B, (long long)B * Lq, Hq, D, s_max);
+  const SplitWorkspace ws = split_workspace_layout(B, Hkv, (long long)B * Lq, Hq, D, s_max);
   if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
                 workspace_bytes);
@@ -545,6 +550,8 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
     c.o_part = p.o_part;
     c.lse_part = p.lse_part;
     c.nsplit = p.nsplit;
+    c.ns_stride = Hkv;
+    c.ns_group = G;
     c.S = s_max;
     c.B = B; c.Lq = Lq; c.Hq = Hq;
     c.cu_seqlens_q = nullptr;
@@ -591,7 +598,7 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
   // packed split-KV items, longer chunks as 128-row tiles of one head.
   const bool pack = (kEngineMaxRows % G) == 0;
   const int s_max = pack ? plan_s_max(B, Hkv, max_seqlen_k, 0) : 1;
-  const SplitWorkspace ws = split_workspace_layout(B, total_q, Hq, D, s_max);
+  const SplitWorkspace ws = split_workspace_layout(B, Hkv, total_q, Hq, D, s_max);
   if (ws.total > 0 && (workspace == nullptr || workspace_bytes < ws.total))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", ws.total,
                 workspace_bytes);
@@ -637,6 +644,8 @@ PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_t
     c.o_part = ep.o_part;
     c.lse_part = ep.lse_part;
     c.nsplit = ep.nsplit;
+    c.ns_stride = 1;
+    c.ns_group = Hq;
     c.S = s_max;
     c.B = B; c.Lq = 0; c.Hq = Hq;
     c.cu_seqlens_q = cu_seqlens_q;
@@ -665,6 +674,8 @@ PA_API int pa_split_combine(const float* o_partial, const float* lse_partial,
   c.o_part = o_partial;
   c.lse_part = lse_partial;
   c.nsplit = splits_per_seq;
+  c.ns_stride = 1;
+  c.ns_group = Hq;
   c.S = S;
   c.B = B; c.Lq = Lq; c.Hq = Hq;
   c.cu_seqlens_q = nullptr;

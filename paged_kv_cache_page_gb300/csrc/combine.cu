@@ -42,17 +42,38 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
       b = (int)(row / p.Lq);
       qi = (int)(row % p.Lq);
     }
-    const int n = p.nsplit ? min(__ldg(p.nsplit + b), p.S) : p.S;
-    if (n <= 0) continue;
-    // max of the split LSEs (natural log) -> log2 domain; lane s keeps the
-    // LSE of split s (and of s + 32, ...)
-    float M = neg_inf();
-    float my_ls = neg_inf();
-    for (int s = lane; s < n; s += 32) {
-      const float ls = __ldg(p.lse_part + ((long long)s * NR + row) * p.Hq + h) * kLog2e;
-      if (s == lane) my_ls = ls;
-      M = fmaxf(M, ls);
+    // The split count, the LSE of split `lane` and the first kU partial
+    // rows are loaded together (every index is below S, the splits the
+    // partial arrays hold) and masked once the count is known: one round
+    // trip to L2 instead of three dependent ones.
+    constexpr int kU = 4;
+    const long long base = (long long)row * p.Hq + h;    // (row, head) of split 0
+    const long long sstride = NR * p.Hq;                 // one split further
+    const int ns = p.nsplit ? __ldg(p.nsplit + (long long)b * p.ns_stride + h / p.ns_group) : p.S;
+    const float ls_lane = lane < p.S ? __ldg(p.lse_part + lane * sstride + base) * kLog2e : neg_inf();
+    float v0[kU][kPVE];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+#pragma unroll
+      for (int e = 0; e < kPVE; ++e) v0[u][e] = 0.f;
+      if (u < p.S) {
+        const float* op = p.o_part + (u * sstride + base) * D + lane * kPVE;
+        if constexpr (kPVE == 4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(op));
+          v0[u][0] = x.x; v0[u][1] = x.y; v0[u][2] = x.z; v0[u][3] = x.w;
+        } else {
+          const float2 x = __ldg(reinterpret_cast<const float2*>(op));
+          v0[u][0] = x.x; v0[u][1] = x.y;
+        }
+      }
     }
+    const int n = min(ns, p.S);
+    if (n <= 0) continue;
+    // max of the split LSEs (natural log -> log2 domain); lane s keeps the
+    // LSE of split s < 32
+    const float my_ls = lane < n ? ls_lane : neg_inf();
+    float M = my_ls;
+    for (int s = lane + 32; s < n; s += 32) M = fmaxf(M, __ldg(p.lse_part + s * sstride + base) * kLog2e);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[kPVE];
@@ -60,41 +81,34 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     for (int e = 0; e < kPVE; ++e) acc[e] = 0.f;
     float L = 0.f;
     if (M != neg_inf()) {
-      // four splits per step: their partial rows are loaded together; an
-      // empty split (LSE -inf) gets weight 0 and its partial is not read
-      constexpr int kU = 4;
-      for (int s0 = 0; s0 < n; s0 += kU) {
-        float wgt[kU];
-        float v[kU][kPVE];
+      // an empty split (LSE -inf) gets weight 0 and its partial row, which
+      // may hold anything, is never used
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int s = s0 + u;
-          float ls = neg_inf();
-          if (s < 32) {
-            ls = __shfl_sync(0xffffffffu, my_ls, s & 31);
-          } else if (s < n) {
-            ls = __ldg(p.lse_part + ((long long)s * NR + row) * p.Hq + h) * kLog2e;
-          }
-          const bool live = s < n && ls != neg_inf();
-          wgt[u] = live ? ex2(ls - M) : 0.f;
-          const float* op = p.o_part + (((long long)s * NR + row) * p.Hq + h) * D + lane * kPVE;
+      for (int u = 0; u < kU; ++u) {
+        const float ls = __shfl_sync(0xffffffffu, my_ls, u);
+        const bool live = u < n && ls != neg_inf();
+        const float wgt = live ? ex2(ls - M) : 0.f;
+        L += wgt;
 #pragma unroll
-          for (int e = 0; e < kPVE; ++e) v[u][e] = 0.f;
-          if (live) {
-            if constexpr (kPVE == 4) {
-              const float4 x = __ldg(reinterpret_cast<const float4*>(op));
-              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-            } else {
-              const float2 x = __ldg(reinterpret_cast<const float2*>(op));
-              v[u][0] = x.x; v[u][1] = x.y;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          L += wgt[u];
-#pragma unroll
-          for (int e = 0; e < kPVE; ++e) acc[e] = fmaf(wgt[u], v[u][e], acc[e]);
+        for (int e = 0; e < kPVE; ++e) acc[e] = live ? fmaf(wgt, v0[u][e], acc[e]) : acc[e];
+      }
+      for (int s = kU; s < n; ++s) {
+        const float ls = s < 32 ? __shfl_sync(0xffffffffu, my_ls, s)
+                                : __ldg(p.lse_part + s * sstride + base) * kLog2e;
+        if (ls == neg_inf()) continue;
+        const float wgt = ex2(ls - M);
+        L += wgt;
+        const float* op = p.o_part + (s * sstride + base) * D + lane * kPVE;
+        if constexpr (kPVE == 4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(op));
+          acc[0] = fmaf(wgt, x.x, acc[0]);
+          acc[1] = fmaf(wgt, x.y, acc[1]);
+          acc[2] = fmaf(wgt, x.z, acc[2]);
+          acc[3] = fmaf(wgt, x.w, acc[3]);
+        } else {
+          const float2 x = __ldg(reinterpret_cast<const float2*>(op));
+          acc[0] = fmaf(wgt, x.x, acc[0]);
+          acc[1] = fmaf(wgt, x.y, acc[1]);
         }
       }
     }
@@ -121,6 +135,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 template <int D, typename T>
 cudaError_t launch_t(const CombineParams& p, long long rows_total, cudaStream_t st,
                      bool dependent) {
+  if (p.nsplit != nullptr && (p.ns_stride < 1 || p.ns_group < 1)) return cudaErrorInvalidValue;
   const long long warps = rows_total * p.Hq;
   long long blocks = (warps + kCombineWarps - 1) / kCombineWarps;
   const long long cap = 152LL * 16;

@@ -231,10 +231,9 @@ __device__ __forceinline__ void patch_new_tokens(const DecodeParams& p, T* kp, T
 //   O^T[D][8 rows] += V^T[D][16] P^T[16][8]     D/16 MMAs per row tile, V^T by
 //                                               ldmatrix.trans
 // The eight warps' (m, l, O) are merged at the end of the item.
-template <int D, typename T, int RMAX, typename ItemOf>
-__device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem, int num_items,
-                                            ItemOf& item_of, int cta, int num_ctas, int warp,
-                                            int lane) {
+template <int D, typename T, int RMAX, typename NextWork, typename Pos>
+__device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem,
+                                            NextWork& next_work, Pos work0, int warp, int lane) {
   using Tr = DecodeTraits<D, T, RMAX>;
   using E = Elem<T>;
   constexpr int NT = RMAX / 8;  // row tiles (MMA N = 8 rows each)
@@ -261,10 +260,10 @@ __device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem
 
   uint32_t qctr = 0;  // stages of earlier items: ring position of this item's first stage
   bool failed = false;
-  for (int item = cta; item < num_items; item += num_ctas) {
-    int b, g, s, nb, p0, p1;
-    SeqInfo si;
-    item_of(item, b, g, s, nb, p0, p1, si);
+  Pos wp = work0;
+  int b, g, s, nb, p0, p1;
+  SeqInfo si;
+  while (next_work(wp, b, g, s, nb, p0, p1, si)) {
     const int R = si.qlen * p.G;  // <= RMAX for every item that exists
     const int kend = min(p1 * kPage, si.lk);
     int lim[NT][2];  // last key position rows n0, n0 + 1 of each tile may attend (-1: none)
@@ -490,6 +489,23 @@ __device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem
   }
 }
 
+// Position of a CTA in its work: the next item index (direct, uniform) or
+// the next page of its share of the concatenated streams (balanced).
+struct WorkPos {
+  int item;
+  int x, x_end;
+};
+
+// Last index i in [0, n) with pre[i] <= x (pre non-decreasing, pre[0] <= x).
+__device__ __forceinline__ int last_le_int(const int* pre, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 template <int D, typename T, int RMAX>
 __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
                                   DecodeTraits<D, T, RMAX>::kMinBlocks)
@@ -528,26 +544,35 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
     tma_prefetch_desc(&tmv);
   }
 
-  // ---- device split schedule: per-sequence split counts and their prefix sum
+  // ---- device work schedule, from the lengths on the GPU (no host read):
+  //   direct    one split per sequence (kvcache call, s_max == 1): item i is
+  //             (b, g) = (i / Hkv, i % Hkv), items dealt to the CTAs in turn.
+  //   uniform   explicit num_splits: every sequence in min(pages, num_splits)
+  //             splits of equal pages, items dealt in turn.
+  //   balanced  automatic splits: the pages of all (sequence, kv head)
+  //             streams, concatenated sequence by sequence, are cut into equal
+  //             contiguous shares of `share` pages, one per CTA; the pieces a
+  //             stream is cut into are its splits (consecutive CTAs).
   const bool direct = p.s_max <= 1 && p.cu_seqlens_q == nullptr;
-  int num_items;
-  int chunk = 0;
+  const bool balanced = !direct && p.target_ctas < kForcedSplitTarget && p.s_max >= 2;
+  int num_items = 0;   // direct, uniform
+  int chunk = 0;       // uniform: pages per split
+  int share = 1;       // balanced: pages per CTA
+  int total_pages = 0; // balanced: pages of all streams
+  const SplitSched sch{p.s_max, p.target_ctas, p.min_chunk_pages};
   if (direct) {
     num_items = p.B * p.Hkv;
   } else {
     // Lengths of every sequence -> shared memory (item decoding reads them
-    // there), pages -> sPrefix (scratch until the prefix sum replaces it) and
-    // the longest sequence (block max).  Then candidate split count i is
-    // costed by warp i, its lanes over the sequences, so the candidates are
-    // evaluated side by side rather than one after another.
-    SplitSched sch{p.s_max, p.target_ctas, p.min_chunk_pages};
-    int* sRed = reinterpret_cast<int*>(sMerge);  // [warp] maxima, then [candidate] costs
+    // there; sLk -1: not handled by this kernel), pages -> sPrefix (scratch
+    // until the prefix sum replaces it), and the longest sequence.
+    int* sRed = reinterpret_cast<int*>(sMerge);
     int pmax = 0;
     for (int b = tid; b < p.B; b += Tr::kThreads) {
       SeqInfo si = seq_info<RMAX>(p, b, true);
       const int pages = si.active ? (si.lk + kPage - 1) / kPage : -1;
       sPrefix[b] = pages;
-      sLk[b] = si.lk;
+      sLk[b] = si.active ? si.lk : -1;
       sOld[b] = si.old;
       pmax = max(pmax, pages);
     }
@@ -557,55 +582,34 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
     __syncthreads();
     pmax = 0;
     for (int w = 0; w < Tr::kThreads / 32; ++w) pmax = max(pmax, sRed[w]);
+    if (!balanced) chunk = max(1, p.min_chunk_pages);
     __syncthreads();
-    if (p.target_ctas >= kForcedSplitTarget) {
-      chunk = max(1, p.min_chunk_pages);
-    } else {
-      static_assert(Tr::kThreads / 32 >= kSplitCands, "one warp per candidate");
-      if (warp < kSplitCands) {
-        const int n_c = split_cand(warp);
-        const int cchunk = split_cand_chunk(sch, pmax, n_c);
-        int cnt = 0;
-        for (int b = lane; b < p.B; b += 32) {
-          const int pages = sPrefix[b];
-          if (pages < 0) continue;
-          int n;
-          split_pages_per(sch, pages, cchunk, &n);
-          cnt += n;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-        if (lane == 0)
-          sRed[warp] = (n_c <= max(1, p.s_max)) ? split_cand_cost(sch, cnt * p.Hkv, cchunk, n_c > 1)
-                                                : 0x7fffffff;
-      }
-      __syncthreads();
-      int best = 0;
-#pragma unroll
-      for (int i = 1; i < kSplitCands; ++i)
-        if (sRed[i] < sRed[best]) best = i;
-      chunk = split_cand_chunk(sch, pmax, split_cand(best));
-      __syncthreads();
-    }
+    // prefix sums over the sequences (warp 0): uniform -> split counts,
+    // balanced -> pages of all kv heads
     if (warp == 0) {
       int carry = 0;
       for (int base = 0; base < p.B; base += 32) {
         const int b = base + lane;
-        int n = 0;
+        int v = 0;
         if (b < p.B) {
           const int pages = sPrefix[b];
-          if (pages >= 0) split_pages_per(sch, pages, chunk, &n);
-          // split count read by the combine step, for every sequence (0: the
-          // sequence's rows are written directly)
-          if (blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
+          if (balanced) {
+            v = max(pages, 0) * p.Hkv;
+          } else if (pages >= 0) {
+            split_pages_per(sch, pages, chunk, &v);
+            // split count read by the combine step for every (sequence, kv
+            // head); 0: the rows are written directly
+            if (blockIdx.x == 0 && p.nsplit != nullptr)
+              for (int g = 0; g < p.Hkv; ++g) p.nsplit[(int64_t)b * p.Hkv + g] = v > 1 ? v : 0;
+          }
         }
-        int incl = n;
+        int incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        if (b < p.B) sPrefix[b] = carry + incl - n;
+        if (b < p.B) sPrefix[b] = carry + incl - v;
         carry += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0) {
@@ -614,57 +618,123 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
       }
     }
     __syncthreads();
-    num_items = sMisc[0] * p.Hkv;
+    if (!balanced) {
+      num_items = sMisc[0] * p.Hkv;
+    } else {
+      total_pages = sMisc[0];
+      // an equal share per CTA, at least min_chunk pages, and large enough
+      // that no stream is cut into more than s_max pieces
+      share = (total_pages + (int)gridDim.x - 1) / (int)gridDim.x;
+      share = max(share, max(p.min_chunk_pages, (pmax + p.s_max - 2) / max(1, p.s_max - 1)));
+      share = max(share, 1);
+      if (blockIdx.x == 0 && p.nsplit != nullptr) {
+        for (int idx = tid; idx < p.B * p.Hkv; idx += Tr::kThreads) {
+          const int b = idx / p.Hkv, g = idx % p.Hkv;
+          const int pages = sLk[b] > 0 ? (sLk[b] + kPage - 1) / kPage : 0;
+          int n = 0;
+          if (pages > 0) {
+            const int start = sPrefix[b] + g * pages;
+            n = (start + pages - 1) / share - start / share + 1;
+          }
+          p.nsplit[idx] = n > 1 ? n : 0;
+        }
+      }
+      // sequences without keys are in no share: their rows (O = 0, LSE =
+      // -inf) are written here, by CTA b mod grid
+      for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (sLk[b] != 0) continue;
+        int qlen = p.Lq;
+        int64_t row0 = (int64_t)b * p.Lq;
+        if (p.cu_seqlens_q != nullptr) {
+          row0 = __ldg(p.cu_seqlens_q + b);
+          qlen = __ldg(p.cu_seqlens_q + b + 1) - (int)row0;
+        }
+        const int nrow = qlen * p.Hq;
+        for (int idx = tid; idx < nrow * (D / 8); idx += Tr::kThreads) {
+          const int r = idx / (D / 8), c = idx % (D / 8);
+          T* dst = reinterpret_cast<T*>(p.out) + (row0 + r / p.Hq) * p.Hq * D + (r % p.Hq) * D + c * 8;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (p.lse != nullptr) {
+          for (int r = tid; r < nrow; r += Tr::kThreads) {
+            const int qi = r / p.Hq, h = r % p.Hq;
+            if (p.cu_seqlens_q != nullptr)
+              p.lse[(int64_t)h * p.total_q + row0 + qi] = neg_inf();
+            else
+              p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = neg_inf();
+          }
+        }
+      }
+    }
   }
   __syncthreads();
 
-  const SplitSched sch{p.s_max, p.target_ctas, p.min_chunk_pages};
-
-  // Work-item decoding shared by producer and consumers.
-  auto item_of = [&](int item, int& b, int& g, int& s, int& nb, int& p0, int& p1, SeqInfo& si) {
-    g = item % p.Hkv;
-    const int j = item / p.Hkv;
-    if (direct) {
-      b = j;
-      s = 0;
-    } else {
-      int lo = 0, hi = p.B;  // find last b with prefix[b] <= j
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (sPrefix[mid] <= j) lo = mid; else hi = mid;
-      }
-      b = lo;
-      s = j - sPrefix[b];
-    }
+  // Work decoding shared by producer and consumers: lengths of a scheduled
+  // sequence from shared memory (validated and reported by the prologue).
+  auto seq_of = [&](int b, SeqInfo& si) {
     if (direct) {
       si = seq_info<RMAX>(p, b, true);
-    } else {
-      // validated (and reported) by the schedule prologue
-      if (p.cu_seqlens_q != nullptr) {
-        const int q0 = __ldg(p.cu_seqlens_q + b);
-        si.qlen = __ldg(p.cu_seqlens_q + b + 1) - q0;
-        si.row0 = q0;
-      } else {
-        si.qlen = p.Lq;
-        si.row0 = (int64_t)b * p.Lq;
-      }
-      si.lk = sLk[b];
-      si.old = sOld[b];
-      si.active = true;
+      return;
     }
-    const int pages = (si.lk + kPage - 1) / kPage;
-    const int per = direct ? pages : split_pages_per(sch, pages, chunk, &nb);
-    if (direct) nb = 1;
-    p0 = s * per;
-    p1 = min(p0 + per, pages);
-    if (p0 > p1) p0 = p1;
+    if (p.cu_seqlens_q != nullptr) {
+      const int q0 = __ldg(p.cu_seqlens_q + b);
+      si.qlen = __ldg(p.cu_seqlens_q + b + 1) - q0;
+      si.row0 = q0;
+    } else {
+      si.qlen = p.Lq;
+      si.row0 = (int64_t)b * p.Lq;
+    }
+    si.lk = sLk[b];
+    si.old = sOld[b];
+    si.active = true;
   };
+  // The next work unit of this CTA: sequence b, kv head g, split s of nb,
+  // pages [p0, p1).  Returns false when the CTA has none left.
+  auto next_work = [&](WorkPos& w, int& b, int& g, int& s, int& nb, int& p0, int& p1,
+                       SeqInfo& si) -> bool {
+    if (!balanced) {
+      if (w.item >= num_items) return false;
+      g = w.item % p.Hkv;
+      const int j = w.item / p.Hkv;
+      w.item += gridDim.x;
+      if (direct) {
+        b = j;
+        s = 0;
+      } else {
+        b = last_le_int(sPrefix, p.B, j);
+        s = j - sPrefix[b];
+      }
+      seq_of(b, si);
+      const int pages = (si.lk + kPage - 1) / kPage;
+      const int per = direct ? pages : split_pages_per(sch, pages, chunk, &nb);
+      if (direct) nb = 1;
+      p0 = s * per;
+      p1 = min(p0 + per, pages);
+      if (p0 > p1) p0 = p1;
+      return true;
+    }
+    if (w.x >= w.x_end) return false;
+    b = last_le_int(sPrefix, p.B, w.x);
+    seq_of(b, si);
+    const int pages = (si.lk + kPage - 1) / kPage;  // > 0: w.x lies in this sequence's streams
+    const int off = w.x - sPrefix[b];
+    g = off / pages;
+    p0 = off - g * pages;
+    p1 = min(pages, p0 + (w.x_end - w.x));
+    const int start = sPrefix[b] + g * pages;
+    s = (int)blockIdx.x - start / share;
+    nb = (start + pages - 1) / share - start / share + 1;
+    w.x += p1 - p0;
+    return true;
+  };
+  WorkPos work0;
+  work0.item = blockIdx.x;
+  work0.x = balanced ? min((int)blockIdx.x * share, total_pages) : 0;
+  work0.x_end = balanced ? min(work0.x + share, total_pages) : 0;
 
   // the combine grid that follows may be scheduled now; it waits on the
   // device for this grid's completion before reading any partial
   griddep_launch_dependents();
-  const int cta = blockIdx.x;
-  const int num_ctas = gridDim.x;
 
   if (warp >= Tr::kConsumerWarps) {
     // ======================= producer warps =======================
@@ -692,10 +762,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
         ok = r.ok ? 1 : 0;
       }
     };
-    for (int item = cta; item < num_items; item += num_ctas) {
-      int b, g, s, nb, p0, p1;
-      SeqInfo si;
-      item_of(item, b, g, s, nb, p0, p1, si);
+    WorkPos wp = work0;
+    int b, g, s, nb, p0, p1;
+    SeqInfo si;
+    while (next_work(wp, b, g, s, nb, p0, p1, si)) {
       int base = p0;
       int cur2, cur3, curok, nxt2, nxt3, nxtok;
       fetch(b, p0 + lane, p1, cur2, cur3, curok);
@@ -775,7 +845,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
   }
 
   if constexpr (Tr::kMma) {
-    mma_consume<D, T, RMAX>(p, smem, num_items, item_of, cta, num_ctas, warp, lane);
+    mma_consume<D, T, RMAX>(p, smem, next_work, work0, warp, lane);
   } else {
     // ======================= consumers =======================
     int stage = 0;
@@ -786,10 +856,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
     const int slot = warp % Tr::kStagePages;  // page of the stage this warp reads
     const int part = warp / Tr::kStagePages;  // which kPartKeys keys of that page
 
-    for (int item = cta; item < num_items; item += num_ctas) {
-      int b, g, s, nb, p0, p1;
-      SeqInfo si;
-      item_of(item, b, g, s, nb, p0, p1, si);
+    WorkPos wp = work0;
+    int b, g, s, nb, p0, p1;
+    SeqInfo si;
+    while (next_work(wp, b, g, s, nb, p0, p1, si)) {
       const int R = si.qlen * p.G;  // <= RMAX for every item that exists
       const int kend = min(p1 * kPage, si.lk);
 

@@ -239,54 +239,19 @@ __device__ __forceinline__ PageRef resolve_page(const CacheGeom& g, int b, int l
 }
 
 // ---------------------------------------------------------------- split-KV schedule
-// Device-side choice of the number of KV splits per sequence (replacing a
-// host heuristic that would need the lengths on the CPU).  All CTAs of a
-// launch evaluate the same function of the same inputs, so they agree.
-//
-//   pages_b   = ceil(Lk_b / 16),  P = max_b pages_b
-//   chunk(n)  = max(min_chunk, ceil(P / n) rounded up to 4 pages)
-//   n_b       = clamp(ceil(pages_b / chunk), 1, s_max)
-//   per_b     = ceil(pages_b / n_b) rounded up to 4 pages; n_b = ceil(pages_b / per_b)
-//   items(n)  = Hkv * sum_b n_b
-//   cost(n)   = ceil(items / target_ctas) * (chunk + 4) + (n > 1 ? 23 : 0)
-// and the candidate n in {1, 2, 3, 4, 6, 8, 12, 16} (<= s_max) of least cost
-// is taken: whole waves of resident CTAs times the pages one work item
-// streams, plus four pages' worth of fixed cost per item and 23 for the
-// partial writes and the combine step of a split (constants fitted to
-// measured paged-decode times over batch 1-64 and 1-4K keys on GB300).
-// With an explicit split count (target_ctas = 2^30, min_chunk = 1) every
-// sequence gets min(pages_b, s_max).
+// Pages per split when a sequence of `pages` pages is cut into splits of at
+// most `chunk` pages (rounded up to 4 pages, at most s_max splits); writes
+// the split count.  With s_max <= 1 (or no pages) there is one split.
 struct SplitSched {
   int s_max;
-  int target_ctas;
-  int min_chunk_pages;
+  int target_ctas;      // kForcedSplitTarget: explicit split count (uniform splits)
+  int min_chunk_pages;  // smallest split (automatic splits)
 };
 
-constexpr int kSplitCands = 8;
 constexpr int kForcedSplitTarget = 1 << 30;
 
 __device__ __forceinline__ int round_up4(int x) { return (x + 3) & ~3; }
 
-__device__ __forceinline__ int split_cand(int i) {
-  return i < 4 ? i + 1 : (i == 4 ? 6 : i == 5 ? 8 : i == 6 ? 12 : 16);
-}
-
-// Chunk size (pages) of candidate split count n for a longest sequence of
-// `pmax` pages.
-__device__ __forceinline__ int split_cand_chunk(const SplitSched& s, int pmax, int n) {
-  int c = round_up4((pmax + n - 1) / n);
-  if (c < s.min_chunk_pages) c = s.min_chunk_pages;
-  return c < 4 ? 4 : c;
-}
-
-// Cost of a candidate in page-times, see above.
-__device__ __forceinline__ int split_cand_cost(const SplitSched& s, int items, int chunk,
-                                               bool split) {
-  const int waves = (items + s.target_ctas - 1) / s.target_ctas;
-  return waves * (chunk + 4) + (split ? 23 : 0);
-}
-
-// Pages per split for a sequence of `pages` pages; writes the split count.
 __device__ __forceinline__ int split_pages_per(const SplitSched& s, int pages, int chunk,
                                                int* n_out) {
   if (s.s_max <= 1 || pages <= 0) {

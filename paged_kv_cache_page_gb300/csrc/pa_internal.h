@@ -43,14 +43,17 @@ struct DecodeParams {
   int grid_ctas;     // persistent CTAs launched (resident capacity)
   float* o_part;     // [s_max, NR, Hq, D] (NR = B*Lq or total_q)
   float* lse_part;   // [s_max, NR, Hq]
-  int32_t* nsplit;   // [B]: splits to combine (0: final output already written)
+  int32_t* nsplit;   // [B, Hkv]: splits to combine per (sequence, kv head); 0: final
+                     // output already written
   int32_t* err;
 };
 
 struct CombineParams {
   const float* o_part;
   const float* lse_part;
-  const int32_t* nsplit;  // null: all S splits valid
+  const int32_t* nsplit;  // null: all S splits valid; else entry
+                          // b * ns_stride + h / ns_group is the split count of (b, h)
+  int ns_stride, ns_group;
   int S, B, Lq, Hq;
   const int32_t* cu_seqlens_q;  // non-null: varlen row addressing
   int total_q;
