@@ -111,14 +111,16 @@ struct SplitWorkspace {
   size_t off_nsplit, off_lse, off_o, total;
 };
 
-// Split workspace: split counts [B, Hkv] (int32), then LSE partials
-// [s_max, rows, Hq] and O partials [s_max, rows, Hq, D] (fp32), each
-// 256-byte aligned.
+// Split workspace: a split-bookkeeping region of 8 bytes per (sequence, kv
+// head) -- the decode kernel's arrival words, or the engine's per-sequence
+// split counts (int32) -- then LSE partials [s_max, rows, Hq] and O partials
+// [s_max, rows, Hq, D] (fp32), each 256-byte aligned.  Nothing in it has to
+// start at any particular value.
 SplitWorkspace split_workspace_layout(int B, int Hkv, long long rows, int Hq, int D, int s_max) {
   SplitWorkspace w{};
   if (s_max <= 1) return w;
   w.off_nsplit = 0;
-  w.off_lse = align256((size_t)B * Hkv * 4);
+  w.off_lse = align256((size_t)B * Hkv * 8);
   w.off_o = w.off_lse + align256((size_t)s_max * rows * Hq * 4);
   w.total = w.off_o + align256((size_t)s_max * rows * Hq * D * 4);
   return w;
@@ -538,29 +540,14 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   p.grid_ctas = resident;
   p.min_chunk_pages = num_splits > 0 ? 1 : kMinChunkPages;
   uint8_t* wsb = reinterpret_cast<uint8_t*>(workspace);
-  p.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
+  p.split_ctr = ws.total ? reinterpret_cast<unsigned long long*>(wsb + ws.off_nsplit) : nullptr;
   p.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
   p.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
   p.err = err_word;
 
-  cudaError_t e = launch_decode(p, tmk, tmv, D, dtype, rmax, st);
+  // one launch: the last split of every stream to finish merges the stream
+  const cudaError_t e = launch_decode(p, tmk, tmv, D, dtype, rmax, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (s_max > 1) {
-    CombineParams c{};
-    c.o_part = p.o_part;
-    c.lse_part = p.lse_part;
-    c.nsplit = p.nsplit;
-    c.ns_stride = Hkv;
-    c.ns_group = G;
-    c.S = s_max;
-    c.B = B; c.Lq = Lq; c.Hq = Hq;
-    c.cu_seqlens_q = nullptr;
-    c.total_q = 0;
-    c.out = out;
-    c.lse = lse;
-    e = launch_combine(c, D, dtype, B * Lq, st, true);
-    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  }
   return PA_OK;
 }
 

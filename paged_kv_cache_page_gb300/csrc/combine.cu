@@ -12,10 +12,15 @@
 namespace pa {
 namespace {
 
-constexpr int kCombineWarps = 8;
+// Four warps per block: small enough (with the register cap below) to be
+// resident beside a decode CTA, so the blocks of a programmatic dependent
+// launch wait on the SMs rather than behind the decode grid.
+constexpr int kCombineWarps = 4;
 
+// At most 56 registers a thread (nine blocks' worth per SM): a 4-warp block
+// then fits in the registers a 10-warp decode CTA of 168 leaves free.
 template <int D, typename T>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineWarps * 32, 9)
     combine_kernel(const CombineParams p, const long long rows_total) {
   using E = Elem<T>;
   constexpr int kPVE = D / 32;
@@ -46,7 +51,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     // rows are loaded together (every index is below S, the splits the
     // partial arrays hold) and masked once the count is known: one round
     // trip to L2 instead of three dependent ones.
-    constexpr int kU = 4;
+    constexpr int kU = kPVE == 4 ? 6 : 8;
     const long long base = (long long)row * p.Hq + h;    // (row, head) of split 0
     const long long sstride = NR * p.Hq;                 // one split further
     const int ns = p.nsplit ? __ldg(p.nsplit + (long long)b * p.ns_stride + h / p.ns_group) : p.S;
@@ -136,6 +141,16 @@ template <int D, typename T>
 cudaError_t launch_t(const CombineParams& p, long long rows_total, cudaStream_t st,
                      bool dependent) {
   if (p.nsplit != nullptr && (p.ns_stride < 1 || p.ns_group < 1)) return cudaErrorInvalidValue;
+  // the shared-memory carveout the decode kernels run with, so that waiting
+  // blocks can share their SMs
+  static bool carveout_set = false;
+  if (!carveout_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        combine_kernel<D, T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set = true;
+  }
   const long long warps = rows_total * p.Hq;
   long long blocks = (warps + kCombineWarps - 1) / kCombineWarps;
   const long long cap = 152LL * 16;

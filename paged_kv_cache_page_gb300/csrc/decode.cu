@@ -19,7 +19,9 @@
 // (16-byte shared loads), fp32 online softmax in the log2 domain, PV with each
 // lane owning D/32 output columns.  The eight warps' (m, l, O) are merged at
 // the end of the item and written either as the final output (one split) or
-// as a normalised partial + LSE for the combine step.
+// as a normalised partial + LSE; the CTA that finishes a stream's last split
+// merges its partials into the final rows (see "split merge" below), so a
+// call is one launch.
 //
 // New tokens of a kvcache call (k=/v= append) are patched into the staged page
 // from k_new/v_new and written to their cache slots by the CTA whose split
@@ -219,6 +221,125 @@ __device__ __forceinline__ void patch_new_tokens(const DecodeParams& p, T* kp, T
   __syncwarp();
 }
 
+// ---------------------------------------------------------------- split merge
+// The splits of a stream (one sequence, one kv head) are merged by the CTA
+// that finishes last, inside this launch: no combine kernel and no state
+// that has to start at zero.  Each stream has a 64-bit arrival word in the
+// workspace holding (launch tag, count).  The launch tag is %gridid, a per-
+// context launch number that every CTA of a grid reads alike, so a word
+// holding arbitrary bytes or left by another launch counts as zero
+// arrivals.  Replays of one CUDA graph may share a tag, so the arrival that
+// completes a stream also resets its word to (tag, 0): every completed call
+// leaves the words it used at zero arrivals for a replay.  The 48 low bits
+// of %gridid are the tag; 16 bits count up to the split count.  No CTA
+// waits on another: the compare-and-swap loop ends after at most as many
+// rounds as there are splits.
+__device__ __forceinline__ unsigned long long launch_tag() {
+  unsigned long long id;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(id));
+  return id & 0xffffffffffffull;
+}
+
+// One arrival on `word` for this launch; true for the arrival that makes
+// `nb` of them, which leaves the word at (tag, 0).
+__device__ __forceinline__ bool arrive_last(unsigned long long* word, unsigned long long tag,
+                                            int nb) {
+  unsigned long long cur = atomicAdd(word, 0ull);
+  for (;;) {
+    const unsigned long long cnt = ((cur >> 16) == tag) ? (cur & 0xffffull) : 0ull;
+    const bool last = cnt + 1 >= (unsigned long long)nb;
+    const unsigned long long want = (tag << 16) | (last ? 0ull : cnt + 1);
+    const unsigned long long prev = atomicCAS(word, cur, want);
+    if (prev == cur) return last;
+    cur = prev;
+  }
+}
+
+// One warp merges the nb split partials of (row, h): O = sum_s w_s O_s / L,
+// w_s = 2^(LSE_s log2 e - M), LSE = (M + log2 L) ln 2.  An empty split
+// (LSE -inf) has weight 0 and its row is not read.
+template <int D, typename T>
+__device__ __forceinline__ void merge_split_row(const DecodeParams& p, int64_t row, int h, int qi,
+                                                int b, int nb, int64_t nrows_all, int lane) {
+  constexpr int kPVE = D / 32;
+  const int64_t base = row * p.Hq + h;
+  const int64_t sstride = nrows_all * p.Hq;
+  float M = neg_inf();
+  float my_ls = neg_inf();
+  for (int s = lane; s < nb; s += 32) {
+    const float ls = __ldcg(p.lse_part + s * sstride + base) * kLog2e;
+    if (s == lane) my_ls = ls;
+    M = fmaxf(M, ls);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[kPVE];
+#pragma unroll
+  for (int e = 0; e < kPVE; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (M != neg_inf()) {
+    for (int s = 0; s < nb; ++s) {
+      const float ls = s < 32 ? __shfl_sync(0xffffffffu, my_ls, s)
+                              : __ldcg(p.lse_part + s * sstride + base) * kLog2e;
+      if (ls == neg_inf()) continue;
+      const float w = ex2(ls - M);
+      L += w;
+      const float* op = p.o_part + (s * sstride + base) * D + lane * kPVE;
+      if constexpr (kPVE == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(op));
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+        acc[2] = fmaf(w, x.z, acc[2]);
+        acc[3] = fmaf(w, x.w, acc[3]);
+      } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(op));
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+      }
+    }
+  }
+  using E = Elem<T>;
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  T* orow = reinterpret_cast<T*>(p.out) + base * D + lane * kPVE;
+  if constexpr (kPVE == 4) {
+    uint2 u;
+    u.x = E::from_f2(acc[0] * inv, acc[1] * inv);
+    u.y = E::from_f2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(orow) = u;
+  } else {
+    *reinterpret_cast<uint32_t*>(orow) = E::from_f2(acc[0] * inv, acc[1] * inv);
+  }
+  if (p.lse != nullptr && lane == 0) {
+    const float lse_v = L > 0.f ? (M + lg2(L)) * kLn2 : neg_inf();
+    if (p.cu_seqlens_q != nullptr)
+      p.lse[(int64_t)h * p.total_q + row] = lse_v;
+    else
+      p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
+  }
+}
+
+// Called by all consumer warps of a CTA once each has written its partial
+// rows of split `s` of stream (b, g): the arrival, and the merge if this
+// split is the last of the stream's nb to finish.  Consumer warp w merges
+// rows w, w + nwarps, ... of the R rows.
+template <int D, typename T>
+__device__ __forceinline__ void finish_split(const DecodeParams& p, int* sflag, int nwarps, int R,
+                                             int b, int g, int nb, int64_t row0, int warp,
+                                             int lane) {
+  __threadfence();  // this thread's partial rows before the arrival
+  named_barrier(1, nwarps * 32);
+  if (warp == 0 && lane == 0)
+    *sflag = arrive_last(p.split_ctr + (int64_t)b * p.Hkv + g, launch_tag(), nb) ? 1 : 0;
+  named_barrier(1, nwarps * 32);
+  if (*sflag == 0) return;
+  __threadfence();  // every split's partial rows are visible past the last arrival
+  const int64_t nrows_all = p.cu_seqlens_q ? (int64_t)p.total_q : (int64_t)p.B * p.Lq;
+  for (int r = warp; r < R; r += nwarps) {
+    const int qi = r / p.G;
+    merge_split_row<D, T>(p, row0 + qi, g * p.G + (r % p.G), qi, b, nb, nrows_all, lane);
+  }
+}
+
 // Tensor-core consumer for 3-16 query rows per kv head (see DecodeTraits).
 // Warp w owns page w % 4 of the stages whose sequence number has parity
 // w / 4; every warp still waits for every stage and releases it (the item's
@@ -246,6 +367,7 @@ __device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Tr::kOffBar);
   uint64_t* empty = full + Tr::kStages;
   const T* sQ = reinterpret_cast<const T*>(smem + Tr::kOffQ);
+  int* sFlag = reinterpret_cast<int*>(smem + Tr::kOffMisc) + 1;
 
   const int k0 = lane >> 2;        // key of accumulator elements 0, 1 (k0 + 8: 2, 3)
   const int n0 = (lane & 3) * 2;   // rows n0, n0 + 1 of each row tile
@@ -485,6 +607,8 @@ __device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem
         }
       }
     }
+    if (to_partial)
+      finish_split<D, T>(p, sFlag, Tr::kConsumerWarps, R, b, g, nb, si.row0, warp, lane);
     named_barrier(1, Tr::kConsumerWarps * 32);
   }
 }
@@ -597,10 +721,6 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
             v = max(pages, 0) * p.Hkv;
           } else if (pages >= 0) {
             split_pages_per(sch, pages, chunk, &v);
-            // split count read by the combine step for every (sequence, kv
-            // head); 0: the rows are written directly
-            if (blockIdx.x == 0 && p.nsplit != nullptr)
-              for (int g = 0; g < p.Hkv; ++g) p.nsplit[(int64_t)b * p.Hkv + g] = v > 1 ? v : 0;
           }
         }
         int incl = v;
@@ -627,18 +747,6 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
       share = (total_pages + (int)gridDim.x - 1) / (int)gridDim.x;
       share = max(share, max(p.min_chunk_pages, (pmax + p.s_max - 2) / max(1, p.s_max - 1)));
       share = max(share, 1);
-      if (blockIdx.x == 0 && p.nsplit != nullptr) {
-        for (int idx = tid; idx < p.B * p.Hkv; idx += Tr::kThreads) {
-          const int b = idx / p.Hkv, g = idx % p.Hkv;
-          const int pages = sLk[b] > 0 ? (sLk[b] + kPage - 1) / kPage : 0;
-          int n = 0;
-          if (pages > 0) {
-            const int start = sPrefix[b] + g * pages;
-            n = (start + pages - 1) / share - start / share + 1;
-          }
-          p.nsplit[idx] = n > 1 ? n : 0;
-        }
-      }
       // sequences without keys are in no share: their rows (O = 0, LSE =
       // -inf) are written here, by CTA b mod grid
       for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -716,12 +824,12 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
     if (w.x >= w.x_end) return false;
     b = last_le_int(sPrefix, p.B, w.x);
     seq_of(b, si);
-    const int pages = (si.lk + kPage - 1) / kPage;  // > 0: w.x lies in this sequence's streams
+    const int pages = (si.lk + kPage - 1) / kPage;  // > 0: w.x lies in this sequence's pages
     const int off = w.x - sPrefix[b];
     g = off / pages;
     p0 = off - g * pages;
-    p1 = min(pages, p0 + (w.x_end - w.x));
     const int start = sPrefix[b] + g * pages;
+    p1 = min(pages, p0 + (w.x_end - w.x));
     s = (int)blockIdx.x - start / share;
     nb = (start + pages - 1) / share - start / share + 1;
     w.x += p1 - p0;
@@ -732,9 +840,6 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
   work0.x = balanced ? min((int)blockIdx.x * share, total_pages) : 0;
   work0.x_end = balanced ? min(work0.x + share, total_pages) : 0;
 
-  // the combine grid that follows may be scheduled now; it waits on the
-  // device for this grid's completion before reading any partial
-  griddep_launch_dependents();
 
   if (warp >= Tr::kConsumerWarps) {
     // ======================= producer warps =======================
@@ -1059,8 +1164,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
         }
       }
       named_barrier(1, Tr::kConsumerWarps * 32);
+      const bool to_partial = nb > 1;
       if (warp == 0) {
-        const bool to_partial = nb > 1;
   #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
           if (r < R) {
@@ -1116,6 +1221,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
           }
         }
       }
+      if (to_partial)
+        finish_split<D, T>(p, sMisc + 1, Tr::kConsumerWarps, R, b, g, nb, si.row0, warp, lane);
       named_barrier(1, Tr::kConsumerWarps * 32);
     }
   }

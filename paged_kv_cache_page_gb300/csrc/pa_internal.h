@@ -43,8 +43,8 @@ struct DecodeParams {
   int grid_ctas;     // persistent CTAs launched (resident capacity)
   float* o_part;     // [s_max, NR, Hq, D] (NR = B*Lq or total_q)
   float* lse_part;   // [s_max, NR, Hq]
-  int32_t* nsplit;   // [B, Hkv]: splits to combine per (sequence, kv head); 0: final
-                     // output already written
+  // [B, Hkv] arrival words of the in-launch split merge: (launch tag, count)
+  unsigned long long* split_ctr;
   int32_t* err;
 };
 
