@@ -23,7 +23,7 @@ SOURCES = ["api.cu", "append.cu", "decode.cu", "combine.cu", "noalloc.cu", "engi
 # Encoding self-test of the tensor-core operand layouts: test infrastructure,
 # kept out of the product library.
 SELFTEST_LIB = "libpa_selftest.so"
-SELFTEST_SOURCES = ["selftest_tcgen05.cu", "selftest_tcgen05_t.cu", "selftest_mma_rate.cu",
+SELFTEST_SOURCES = ["selftest_tcgen05.cu", "selftest_tcgen05_t.cu",
                     "selftest_timeout.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
