@@ -193,10 +193,14 @@ PA_API size_t pa_fwd_kvcache_workspace_size(int B, int Lq, int Hq, int Hkv, int 
  *                           PA_DEVERR_LENGTH (sequence, position) in err_word.
  *   rotary_dim              even, 2 <= rotary_dim <= D.
  * Requires Lnew >= 1 (the rotation applies to appended tokens).  workspace:
- * pa_fwd_kvcache_rotary_workspace_size bytes, 256-byte aligned (the rotated q
- * and k_new live there for the call, ahead of pa_fwd_kvcache's own scratch).
- * Runs one extra kernel (the rotation) ahead of the pa_fwd_kvcache launches on
- * `stream`; same return codes as pa_fwd_kvcache.
+ * pa_fwd_kvcache_rotary_workspace_size bytes, 256-byte aligned.
+ * Query blocks of up to 16 rows per kv head (Lq * Hq / Hkv <= 16: decode,
+ * GQA decode, short multi-query decode) are rotated inside the attention
+ * launch: q as it is staged for the kernel, k_new where the fused append
+ * stores it; the workspace is then pa_fwd_kvcache's own.  Longer query
+ * blocks run one extra kernel (the rotation into the workspace, ahead of
+ * pa_fwd_kvcache's own scratch) before the attention launches.  Same return
+ * codes as pa_fwd_kvcache.
  */
 PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
                                  pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,

@@ -230,6 +230,30 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int dtype, int D, int 
 
 using namespace pa;
 
+// Rotary embedding applied inside the decode kernel (query blocks of up to
+// kCudaCoreRows rows per kv head): tables, dimensions, pairing.
+struct RopeArgs {
+  const void* cos;
+  const void* sin;
+  int len, dim, interleaved;
+};
+
+static int fwd_kvcache_impl(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                            pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                            const void* v_new, int Lnew, const int32_t* cache_seqlens,
+                            const int32_t* block_table, int64_t bt_stride, int max_pages,
+                            int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                            int64_t cache_extent, int max_seqlen_k, float scale, int causal,
+                            int num_splits, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* err_word, int dtype,
+                            pa_stream_t stream, const RopeArgs* rope);
+
+// Whether pa_fwd_kvcache_rotary rotates inside the attention launch (no
+// scratch, no extra kernel): query blocks the decode kernel runs.
+static bool rotary_fused(int Lq, int Hq, int Hkv) {
+  return Hkv > 0 && Hq % Hkv == 0 && Lq * (Hq / Hkv) <= kCudaCoreRows;
+}
+
 extern "C" {
 
 PA_API const char* pa_last_error_string(void) { return g_last_error.c_str(); }
@@ -298,6 +322,8 @@ static size_t rotary_scratch_bytes(int B, int Lq, int Hq, int Hkv, int D, int Ln
 PA_API size_t pa_fwd_kvcache_rotary_workspace_size(int B, int Lq, int Hq, int Hkv, int D, int Lnew,
                                                    int max_seqlen_k, int num_splits) {
   if (B <= 0 || Lq <= 0 || Lnew <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 0;
+  if (rotary_fused(Lq, Hq, Hkv))
+    return pa_fwd_kvcache_workspace_size(B, Lq, Hq, Hkv, D, max_seqlen_k, num_splits);
   return rotary_scratch_bytes(B, Lq, Hq, Hkv, D, Lnew) +
          pa_fwd_kvcache_workspace_size(B, Lq, Hq, Hkv, D, max_seqlen_k, num_splits);
 }
@@ -325,6 +351,14 @@ PA_API int pa_fwd_kvcache_rotary(const void* q, int64_t q_sb, int64_t q_st, int6
     return fail(PA_ERR_INVALID_ARG, "q, rotary_cos and rotary_sin must be non-NULL");
   if (rotary_dim < 2 || rotary_dim > D || rotary_dim % 2 != 0 || rotary_len < 1)
     return fail(PA_ERR_INVALID_ARG, "rotary_dim must be even in [2, D] and rotary_len >= 1");
+  if (rotary_fused(Lq, Hq, Hkv)) {
+    // the decode kernel rotates q as it stages it and k_new where it appends it
+    const RopeArgs rope{rotary_cos, rotary_sin, rotary_len, rotary_dim, rotary_interleaved ? 1 : 0};
+    return fwd_kvcache_impl(q, q_sb, q_st, q_sh, k_cache, v_cache, k_new, v_new, Lnew,
+                            cache_seqlens, block_table, bt_stride, max_pages, page_size, B, Lq, Hq,
+                            Hkv, D, cache_extent, max_seqlen_k, scale, causal, num_splits, out, lse,
+                            workspace, workspace_bytes, err_word, dtype, stream, &rope);
+  }
   const size_t scratch = rotary_scratch_bytes(B, Lq, Hq, Hkv, D, Lnew);
   if (workspace == nullptr || workspace_bytes < scratch ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -375,6 +409,23 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
                           float scale, int causal, int num_splits, void* out, float* lse,
                           void* workspace, size_t workspace_bytes, int32_t* err_word, int dtype,
                           pa_stream_t stream) {
+  return fwd_kvcache_impl(q, q_sb, q_st, q_sh, k_cache, v_cache, k_new, v_new, Lnew,
+                          cache_seqlens, block_table, bt_stride, max_pages, page_size, B, Lq, Hq,
+                          Hkv, D, cache_extent, max_seqlen_k, scale, causal, num_splits, out, lse,
+                          workspace, workspace_bytes, err_word, dtype, stream, nullptr);
+}
+
+}  // extern "C"
+
+static int fwd_kvcache_impl(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                            pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
+                            const void* v_new, int Lnew, const int32_t* cache_seqlens,
+                            const int32_t* block_table, int64_t bt_stride, int max_pages,
+                            int page_size, int B, int Lq, int Hq, int Hkv, int D,
+                            int64_t cache_extent, int max_seqlen_k, float scale, int causal,
+                            int num_splits, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, int32_t* err_word, int dtype,
+                            pa_stream_t stream, const RopeArgs* rope) {
   int rc = check_common(dtype, D, Hq, Hkv);
   if (rc) return rc;
   if (B < 0 || Lq < 0 || Lnew < 0 || max_seqlen_k < 0 || num_splits < 0)
@@ -408,6 +459,9 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   const int G = Hq / Hkv;
   const int rows = Lq * G;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (rope != nullptr && (rows > kCudaCoreRows || Lnew < 1))
+    return fail(PA_ERR_INVALID_ARG, "in-kernel rotary embedding needs an append and <= %d rows",
+                kCudaCoreRows);
   if (rows > kCudaCoreRows) {
     // Tensor-core engine: the new tokens are appended first (same stream),
     // then every key is read from the cache.  Query blocks of up to 128 rows
@@ -544,12 +598,21 @@ PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_s
   p.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
   p.o_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_o) : nullptr;
   p.err = err_word;
+  if (rope != nullptr) {
+    p.rot_cos = rope->cos;
+    p.rot_sin = rope->sin;
+    p.rot_len = rope->len;
+    p.rot_dim = rope->dim;
+    p.rot_interleaved = rope->interleaved;
+  }
 
   // one launch: the last split of every stream to finish merges the stream
   const cudaError_t e = launch_decode(p, tmk, tmv, D, dtype, rmax, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PA_OK;
 }
+
+extern "C" {
 
 PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_tensor4 k_cache,
                                  pa_tensor4 v_cache, const int32_t* cu_seqlens_q,

@@ -190,9 +190,51 @@ __device__ __forceinline__ int page_elem(int t, int c) {
     return t * D + c * 8;
 }
 
+// Rotary embedding (RoFormer rotation, tables from the caller) of feature d
+// of a new token's row x at position pos: the pair (x1, x2) of d becomes
+// (x1 c - x2 s, x1 s + x2 c), computed in fp32 (each product of two 16-bit
+// values is exact there) and rounded once to the storage type, as the
+// rotated value is stored (k) or attended (q).  Features at or past rot_dim
+// and positions outside the table (`ok` false; reported by the caller) pass
+// through.
+template <typename T>
+__device__ __forceinline__ float rope_elem(const DecodeParams& p, const T* x, int d, int pos,
+                                           bool ok) {
+  if (!ok || d >= p.rot_dim) return static_cast<float>(x[d]);
+  const int half = p.rot_dim >> 1;
+  int q, i1, i2;
+  bool first;
+  if (p.rot_interleaved) {
+    q = d >> 1;
+    i1 = 2 * q;
+    i2 = i1 + 1;
+    first = (d & 1) == 0;
+  } else {
+    first = d < half;
+    q = first ? d : d - half;
+    i1 = q;
+    i2 = q + half;
+  }
+  const float x1 = static_cast<float>(x[i1]);
+  const float x2 = static_cast<float>(x[i2]);
+  const float c = static_cast<float>(__ldg(reinterpret_cast<const T*>(p.rot_cos) + (int64_t)pos * half + q));
+  const float sn = static_cast<float>(__ldg(reinterpret_cast<const T*>(p.rot_sin) + (int64_t)pos * half + q));
+  const float y = first ? fmaf(x1, c, -(x2 * sn)) : fmaf(x1, sn, x2 * c);
+  return static_cast<float>(Elem<T>::from_f(y));
+}
+
+// Whether position pos of sequence b is inside the rotary table; reports it
+// (lane 0 of the caller's warp) when it is not.
+__device__ __forceinline__ bool rope_pos_ok(const DecodeParams& p, int b, int pos, bool report_it) {
+  const bool ok = pos >= 0 && pos < p.rot_len;
+  if (!ok && report_it) report(p.err, PA_DEVERR_LENGTH, b, pos);
+  return ok;
+}
+
 // New tokens of a kvcache call among keys [t0, t1) of a staged page: the
-// staged copy is patched from k_new/v_new and the tokens are written to their
-// cache slots (each consumer warp patches only the keys it reads).
+// staged copy is patched from k_new/v_new (k rotated at its position when the
+// call has rotary embedding) and the tokens are written to their cache slots
+// (each consumer warp patches only the keys it reads).
 template <int D, typename T, bool kSwz>
 __device__ __forceinline__ void patch_new_tokens(const DecodeParams& p, T* kp, T* vp,
                                                  const int* info, int b, int g, int t_base,
@@ -204,8 +246,19 @@ __device__ __forceinline__ void patch_new_tokens(const DecodeParams& p, T* kp, T
     const int t = t0 + idx / kChunks;
     const int c = idx % kChunks;
     const int64_t src = (((int64_t)b * p.Lnew + (t_base + t - old)) * p.Hkv + g) * D + c * 8;
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k_new) + src));
+    uint4 kv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k_new) + src));
     const uint4 vv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v_new) + src));
+    if (p.rot_cos != nullptr && c * 8 < p.rot_dim) {
+      const int pos = t_base + t;
+      const bool rok = rope_pos_ok(p, b, pos, true);
+      const T* krow = reinterpret_cast<const T*>(p.k_new) + (src - c * 8);
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w4[e] = Elem<T>::from_f2(rope_elem<T>(p, krow, c * 8 + 2 * e, pos, rok),
+                                 rope_elem<T>(p, krow, c * 8 + 2 * e + 1, pos, rok));
+      kv = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
     *reinterpret_cast<uint4*>(kp + page_elem<D, kSwz>(t, c)) = kv;
     *reinterpret_cast<uint4*>(vp + page_elem<D, kSwz>(t, c)) = vv;
     if (ok) {
@@ -906,13 +959,21 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
           info[2] = ok;
         }
         __syncwarp();
-        // the item's query rows travel with its first stage
+        // the item's query rows travel with its first stage: bulk-copied, or
+        // with rotary embedding rotated by this warp, which then arrives
+        // after writing them (the transaction bytes are announced first)
         const int nq = (pg == p0 && pw == 0) ? si.qlen * p.G : 0;
-        if (lane == 0)
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(n * Tr::kTensorsPerProducer * Tr::kPageBytes +
-                                                         nq * Tr::kQRowBytes));
+        const bool rot_q = nq > 0 && p.rot_cos != nullptr;
+        if (lane == 0) {
+          const uint32_t tx = (uint32_t)(n * Tr::kTensorsPerProducer * Tr::kPageBytes +
+                                         (rot_q ? 0 : nq * Tr::kQRowBytes));
+          if (rot_q)
+            mbar_expect_tx(&full[stage], tx);
+          else
+            mbar_arrive_expect_tx(&full[stage], tx);
+        }
         __syncwarp();
-        if (lane < nq) {
+        if (!rot_q && lane < nq) {
           const int qi = lane / p.G;
           const int h = g * p.G + (lane % p.G);
           const T* qrow =
@@ -927,6 +988,38 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
           T* dst = (is_k ? sK : sV) + (stage * Tr::kStagePages + w) * Tr::kPageElems +
                    half * (kPage * 64);
           tma_load_4d(dst, is_k ? &tmk : &tmv, &full[stage], half * 64, g, c2, c3, pol);
+        }
+        if (rot_q) {
+          // element e = r * D + d of the rows; four independent elements per
+          // lane at a time, so that their loads overlap
+          for (int e0 = 0; e0 < nq * D; e0 += 4 * 32) {
+            float y[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int e = e0 + j * 32 + lane;
+              const int r = e / D, d = e % D;
+              y[j] = 0.f;
+              if (e < nq * D) {
+                const int qi = r / p.G;
+                const int h = g * p.G + (r % p.G);
+                const T* qrow = p.cu_seqlens_q != nullptr
+                                    ? reinterpret_cast<const T*>(p.q) + (si.row0 + qi) * p.q_st +
+                                          (int64_t)h * p.q_sh
+                                    : reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb +
+                                          (int64_t)qi * p.q_st + (int64_t)h * p.q_sh;
+                // query row qi is the (Lnew - Lq + qi)-th new token
+                const int pos = si.old + p.Lnew - si.qlen + qi;
+                y[j] = rope_elem<T>(p, qrow, d, pos, rope_pos_ok(p, b, pos, d == 0));
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int e = e0 + j * 32 + lane;
+              if (e < nq * D) sQ[(stage * RMAX + e / D) * D + e % D] = E::from_f(y[j]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[stage]);
         }
         if (++stage == Tr::kStages) {
           stage = 0;
@@ -1021,33 +1114,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
           // New tokens among this warp's keys: patch the staged copy and append
           // them to the cache (each warp patches only the rows it reads).
           const int kb = part * Tr::kPartKeys;
-          if (p.Lnew > 0 && t_base + min(nvalid, kb + Tr::kPartKeys) > si.old) {
-            const int* info = sInfo + (stage * Tr::kStagePages + slot) * 3;
-            const int c2 = info[0], c3 = info[1];
-            const bool ok = info[2] != 0;
-            const int t0 = max(si.old - t_base, kb);
-            const int t1 = min(nvalid, kb + Tr::kPartKeys);
-            constexpr int kChunks = D / 8;  // 16-byte chunks per row
-            for (int idx = lane; idx < (t1 - t0) * kChunks; idx += 32) {
-              const int t = t0 + idx / kChunks;
-              const int c = idx % kChunks;
-              const int64_t src = (((int64_t)b * p.Lnew + (t_base + t - si.old)) * p.Hkv + g) * D + c * 8;
-              const uint4 kv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k_new) + src));
-              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v_new) + src));
-              *reinterpret_cast<uint4*>(kp + t * D + c * 8) = kv;
-              *reinterpret_cast<uint4*>(vp + t * D + c * 8) = vv;
-              if (ok) {
-                T* kdst = reinterpret_cast<T*>(p.k_cache) + (int64_t)c3 * p.k_sb +
-                          (int64_t)(c2 + t) * p.k_st + (int64_t)g * p.k_sh + c * 8;
-                T* vdst = reinterpret_cast<T*>(p.v_cache) + (int64_t)c3 * p.v_sb +
-                          (int64_t)(c2 + t) * p.v_st + (int64_t)g * p.v_sh + c * 8;
-                *reinterpret_cast<uint4*>(kdst) = kv;
-                *reinterpret_cast<uint4*>(vdst) = vv;
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
+          if (p.Lnew > 0 && t_base + min(nvalid, kb + Tr::kPartKeys) > si.old)
+            patch_new_tokens<D, T, false>(p, kp, vp, sInfo + (stage * Tr::kStagePages + slot) * 3,
+                                          b, g, t_base, si.old, max(si.old - t_base, kb),
+                                          min(nvalid, kb + Tr::kPartKeys), lane);
 
           // ---- S = q K^T for this warp's keys of the page (passes of 4 keys)
           constexpr int kPasses = Tr::kPartKeys / 4;

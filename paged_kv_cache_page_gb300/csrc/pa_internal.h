@@ -46,6 +46,13 @@ struct DecodeParams {
   // [B, Hkv] arrival words of the in-launch split merge: (launch tag, count)
   unsigned long long* split_ctr;
   int32_t* err;
+  // rotary embedding of the new tokens (rot_cos == null: none): features
+  // [0, rot_dim) of q and of k_new rotated at their positions, pairs
+  // (p, p + rot_dim / 2) or, interleaved, (2p, 2p + 1); tables
+  // [rot_len, rot_dim / 2] of the q dtype
+  const void* rot_cos;
+  const void* rot_sin;
+  int rot_dim, rot_len, rot_interleaved;
 };
 
 struct CombineParams {

@@ -75,8 +75,8 @@ def run_case(w, rotary_dim, interleaved, causal, n_pos=None):
 
 
 @pytest.mark.parametrize("dtype,hq,hkv,rotary_dim,interleaved", [
-    ("f16", 8, 8, 128, False),    # MHA decode: the fused decode kernel's append path
-    ("bf16", 16, 4, 64, True),    # GQA decode, partial rotary_dim: the engine path
+    ("f16", 8, 8, 128, False),    # MHA decode: rotated inside the decode launch
+    ("bf16", 16, 4, 64, True),    # GQA decode, partial rotary_dim: tensor-core decode consumer
 ])
 def test_rotary_decode(dtype, hq, hkv, rotary_dim, interleaved):
     w = wl.paged_decode(batch=5, ctx=0, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
@@ -107,3 +107,15 @@ def test_rotary_position_beyond_table_reports():
     torch.cuda.synchronize()
     e = err.tolist()
     assert e[0] == 2 and e[1] == 1 and e[2] == 199, e
+
+
+@pytest.mark.parametrize("lq,hq,hkv,d,dtype,interleaved", [(2, 32, 8, 128, "bf16", False),
+                                                           (4, 16, 4, 64, "f16", True)])
+def test_rotary_short_multi_query_decode_in_launch(lq, hq, hkv, d, dtype, interleaved):
+    """Up to 16 query rows per kv head: rotated inside the decode launch (q as
+    the producer stages it, k where the append stores it), causal among the
+    new tokens, ragged lengths that split."""
+    w = wl.paged_decode(batch=4, ctx=0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                        dtype=dtype, lnew=lq, seed=920 + lq, device=DEV,
+                        lens=[lq, 45, 1500, 3000])
+    run_case(w, d if interleaved else d // 2, interleaved, causal=True)
