@@ -27,8 +27,8 @@
  *     Softmax statistics, partial outputs and LSE are fp32.  LSE is the
  *     natural-log log-sum-exp of the scaled scores; rows with no visible key
  *     produce O = 0 and LSE = -inf.
- *   - head_dim D must be 64 or 128; page size is fixed at 16 tokens;
- *     Hq must be a multiple of Hkv.
+ *   - head_dim D must be 64 or 128; a paged cache's page size is 16, 32, 64,
+ *     128 or 256 tokens (page_size argument); Hq must be a multiple of Hkv.
  *   - Cache tensors are described by pa_tensor4 (element strides; the D axis
  *     is contiguous).  Base pointers must be 16-byte aligned and all three
  *     strides multiples of 8 elements (16 bytes), because K/V tiles are
@@ -151,8 +151,15 @@ PA_API int pa_append_kv(pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_ne
  *   workspace    device scratch of pa_fwd_kvcache_workspace_size(...) bytes
  *                (may be NULL when that size is 0).  Its contents on entry do
  *                not matter.
- * Lq * (Hq/Hkv) <= 8 runs the split-KV decode kernel; larger query blocks run
- * the tensor-core (tcgen05) prefill kernel.
+ * Which kernel runs depends on the query rows per kv head, Lq * (Hq / Hkv):
+ *   <= 2     the split-KV decode kernel, CUDA-core consumers;
+ *   3 - 16   the split-KV decode kernel, warp-level tensor-core consumer;
+ *   17 - 128 the tcgen05 engine, all query heads of a kv head packed in one
+ *            tile, split-KV, followed by the combine kernel when it splits;
+ *   > 128    the tcgen05 prefill kernel, two 128-row query tiles per CTA.
+ * The decode kernel appends k_new / v_new in the same launch and merges its
+ * splits in the same launch (one launch per call); the engine and prefill
+ * paths run the append kernel first.
  */
 PA_API int pa_fwd_kvcache(const void* q, int64_t q_sb, int64_t q_st, int64_t q_sh,
                           pa_tensor4 k_cache, pa_tensor4 v_cache, const void* k_new,
@@ -229,14 +236,16 @@ PA_API size_t pa_fwd_kvcache_rotary_workspace_size(int B, int Lq, int Hq, int Hk
  * the driver's allocator.  They can pass inputs and outputs but not the
  * split-KV scratch that pa_fwd_kvcache takes as `workspace`.  This variant
  * takes the same arguments minus the workspace and uses a fixed scratch array
- * of PA_NOALLOC_SCRATCH_BYTES that every GPU loading the library reserves
- * until the process exits.  It calls no allocating routine.
+ * of PA_NOALLOC_SCRATCH_BYTES that every GPU using the library holds until the
+ * process exits.  It calls no allocating routine.
  *
  *   - Sizes whose split scratch (pa_fwd_kvcache_workspace_size) exceeds
  *     PA_NOALLOC_SCRATCH_BYTES are rejected with PA_ERR_WORKSPACE.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     per device, with that device current).  Under CUDA's lazy module
+ *     loading that lookup may load the library's device code on that device,
+ *     which allocates in the driver (the array included): make the first call
+ *     during set-up -- outside allocator hooks and before any stream capture.
  *   - All calls share the array, which keeps the last call's contents; no
  *     entry needs to start at zero.  Calls whose kernels overlap on the GPU
  *     (other streams, other threads) race on it: serialise them.

@@ -242,6 +242,11 @@ def pa_fwd_kvcache_noalloc(q, k_cache, v_cache, cache_seqlens, out, block_table=
     B, lq, hq, d = q.shape
     hkv = k_cache.shape[2]
     lnew = 0 if k is None else k.shape[1]
+    # the library reads k/v as contiguous [B, Lnew, Hkv, D]; a strided view
+    # cannot be copied here (this call allocates nothing), so it is refused
+    for name, t in (("k", k), ("v", v)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"pa_fwd_kvcache_noalloc: {name} must be contiguous")
     if block_table is not None:
         extent, max_pages, bt_stride = k_cache.shape[0], block_table.shape[1], block_table.stride(0)
         cap = max_pages * k_cache.shape[1]

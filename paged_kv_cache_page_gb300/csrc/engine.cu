@@ -14,7 +14,7 @@
 // A varlen batch may mix both kinds in one launch: the unified launch of vLLM
 // #6052 "Unify the kernel used in flash attention backend".
 //
-// CTA = 416 threads, one per SM, persistent over items:
+// CTA = 512 threads (16 warps), one per SM, persistent over items:
 //   warps 0-7  softmax: warps w and w+4 share tile rows 32(w%4).. (their TMEM
 //              lane quarter), each taking 64 of the 128 columns.  S from TMEM,
 //              masking, running max / sum in the log2 domain, P (fp16/bf16)

@@ -8,15 +8,19 @@
 // pass its own inputs and outputs but cannot provide the split-KV scratch that
 // pa_fwd_kvcache takes as `workspace`.
 //
-// Here that scratch is a fixed array in device memory, reserved when the
-// library is loaded (every GPU that loads the library holds
-// PA_NOALLOC_SCRATCH_BYTES of it until the process exits).  The entry point
-// itself calls no cudaMalloc, cudaFree or allocating library routine.
+// Here that scratch is a fixed array in device memory: every GPU on which the
+// library's device code is loaded holds PA_NOALLOC_SCRATCH_BYTES of it until
+// the process exits.  The entry point itself calls no cudaMalloc, cudaFree or
+// allocating library routine.
 //
 // Host code cannot use the array's name as a device pointer (on the host it
 // names a shadow object), so the device address is looked up once per device
 // with cudaGetSymbolAddress, with that device current, on the first call made
-// on it; that first call should therefore come before any stream capture.
+// on it.  With CUDA's lazy module loading (the default) that lookup may be
+// what loads the library's device code on the device, and loading allocates
+// in the driver, the array included.  The first call on each device should
+// therefore be made during set-up: outside any allocator hook and before any
+// stream capture.
 //
 // All calls share the one array and it keeps the last call's contents.
 // Nothing in it has to start at zero (each call writes every scratch entry it

@@ -8,7 +8,7 @@
 
 namespace pa {
 
-constexpr int kEngineMaxB = 512;   // sequences a launch with a per-sequence schedule may hold
+constexpr int kEngineMaxB = 4096;  // sequences a launch with a per-sequence schedule may hold
 constexpr int kEngineMaxRows = 128;
 
 struct EngineParams {

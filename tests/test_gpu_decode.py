@@ -203,9 +203,11 @@ def test_lengths_beyond_table_report():
 
 def test_full_size_decode_sweep_point_sampled():
     """ctx 4096 x batch 256, 32/32 heads, D 128, fp16 with one appended token:
-    the launch configuration the benchmark times; 6 sequences checked."""
+    the launch configuration the benchmark times; the first and the last 8
+    sequences (the first and the last work items the persistent grid deals)
+    and two in between are checked."""
     w = wl.paged_decode(256, 4096, lnew=1, seed=1002, device=DEV)
-    rows = [0, 1, 77, 128, 200, 255]
+    rows = list(range(8)) + [77, 128] + list(range(248, 256))
     ref_o, ref_l = oracle_kvcache(w, rows=rows)
     out, lse = run(w)
     assert_close(out, lse, ref_o, ref_l, "f16", rows=rows)
@@ -232,3 +234,26 @@ def test_gqa_rows_share_each_key(dtype, d, hq, hkv, lq, splits):
     expect, _ = oracle.append_kv(bits(kc0), bits(kc0), kn, kn, w["cache_seqlens"].cpu().numpy(),
                                  table)
     assert np.array_equal(bits(w["k_cache"]), expect)
+
+
+def test_speculative_decode_bench_shape_sampled():
+    """The multi-query (speculative) decode the benchmark times: 64 sequences
+    at ctx 4096, 6 new tokens appended in the call and attended causally, GQA
+    32/8, D 128, bf16 (query blocks of 24 rows per kv head: the tensor-core
+    engine).  The first and the last 4 sequences are checked against the
+    oracle, and their appended slots bit for bit."""
+    w = wl.paged_decode(batch=64, ctx=4096, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        dtype="bf16", lnew=6, seed=1010, device=DEV)
+    w["causal"] = True
+    rows = [0, 1, 2, 3, 60, 61, 62, 63]
+    ref_o, ref_l = oracle_kvcache(w, rows=rows)
+    out, lse = run(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", rows=rows)
+    table = w["block_table"]
+    for b in rows:
+        old = int(w["cache_seqlens"][b])
+        for i in range(6):
+            pos = old + i
+            page = table[b, pos // 16].long()
+            assert torch.equal(w["k_cache"][page, pos % 16], w["k_new"][b, i])
+            assert torch.equal(w["v_cache"][page, pos % 16], w["v_new"][b, i])

@@ -3,8 +3,9 @@
 The unified launch's grid depends only on host-known capacities (the batch
 entry count, max_seqlen_q, max_seqlen_k, total_q); every length, split count
 and page lives on the device.  So one captured graph serves any batch that
-fits the capacities, padding entries included -- the fixed-capacity unified
-kernel of "vLLM Triton backend deep dive" (CUDA graphs section).  These tests
+fits the capacities, padding entries included -- vLLM #6052 "Unify the
+kernel used in flash attention backend", the comment on CUDA graphs padding
+the batch to the captured size with empty entries.  These tests
 capture once, then rewrite lengths, tables and inputs in place and replay: the
 replay must match the oracle on the new batch and be bit-identical to an eager
 call on the same buffers."""

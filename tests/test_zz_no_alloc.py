@@ -4,10 +4,14 @@ Callers that run inside another library's allocator or stream callback, or in
 a serving process whose device memory pool is owned and capped by the
 framework, cannot hand the library a workspace.  This entry point uses the
 library's own fixed split scratch instead.  The test calls it through the C
-ABI (ctypes, raw arguments) on workloads that do split the keys, twice in a
-row, and checks each result against pa_fwd_kvcache with a caller workspace,
-within the parity tolerances of the other GPU tests.  It lives in its own
-file, named to be collected last.
+ABI (ctypes, raw arguments) on workloads that do split the keys -- the
+tensor-core decode consumer on a contiguous cache, 4 and 1 rows per kv head
+on paged caches with forced split counts -- twice, with a different workload
+run through the same scratch in between (so the second call starts from
+another call's leftovers), and checks each result against pa_fwd_kvcache
+with a caller workspace, within the parity tolerances of the other GPU
+tests.  It also calls the binding's wrapper.  It lives in its own file,
+named to be collected last.
 """
 
 import ctypes
@@ -68,7 +72,29 @@ def _paged_forced_splits():
     return w, "f16"
 
 
-@pytest.mark.parametrize("make,num_splits", [(_contiguous_gqa, 0), (_paged_forced_splits, 7)])
+def _paged_mha_forced_splits():
+    # one query row per kv head: the CUDA-core decode consumer
+    w = wl.paged_decode(4, 0, num_q_heads=8, num_kv_heads=8, head_dim=64,
+                        lens=[513, 2000, 48, 1200], lnew=1, seed=23, device=DEV, dtype="bf16")
+    return w, "bf16"
+
+
+def _interloper():
+    """A different workload (other lengths, heads and split count) run through
+    the same scratch between the two compared calls, so the second one starts
+    from another call's leftovers."""
+    w = wl.paged_decode(3, 0, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                        lens=[3000, 77, 1500], lnew=1, seed=29, device=DEV)
+    out = torch.empty_like(w["q"])
+    lse = torch.empty((3, 16, 1), dtype=torch.float32, device=DEV)
+    err = pa.new_err_word(DEV)
+    assert _raw_noalloc(w, out, lse, err, 5) == pa.PA_OK
+    torch.cuda.synchronize()
+    assert err[0].item() == 0
+
+
+@pytest.mark.parametrize("make,num_splits", [(_contiguous_gqa, 0), (_paged_forced_splits, 7),
+                                             (_paged_mha_forced_splits, 6)])
 def test_noalloc_matches_workspace_entry_point_twice(make, num_splits):
     w, dt = make()
     B, lq, hq, d = w["q"].shape
@@ -77,12 +103,19 @@ def test_noalloc_matches_workspace_entry_point_twice(make, num_splits):
     max_k = (w["block_table"].shape[1] * 16 if w["block_table"] is not None
              else w["k_cache"].shape[1])
     assert pa.fwd_kvcache_workspace_size(B, lq, hq, hkv, d, max_k, num_splits) > 0
+    kc0, vc0 = w["k_cache"].clone(), w["v_cache"].clone()
     ref_out, ref_lse = pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"],
                                          w["cache_seqlens"], w["block_table"],
                                          k=w.get("k_new"), v=w.get("v_new"), scale=w["scale"],
                                          causal=w["causal"], num_splits=num_splits)
     torch.cuda.synchronize()
     for call in range(2):
+        if call == 1:
+            _interloper()
+        # the same cache image before every call (the append writes the same
+        # bytes again)
+        w["k_cache"].copy_(kc0)
+        w["v_cache"].copy_(vc0)
         out = torch.full_like(ref_out, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
         err = pa.new_err_word(DEV)
@@ -98,17 +131,45 @@ def test_noalloc_matches_workspace_entry_point_twice(make, num_splits):
         assert l_err <= LSE_TOL, (call, l_err)
 
 
+def test_noalloc_python_wrapper():
+    """The binding's wrapper passes the caller's tensors through unchanged and
+    refuses a strided k it could only copy by allocating."""
+    w, dt = _paged_forced_splits()
+    out = torch.empty_like(w["q"])
+    lse = torch.empty((w["q"].shape[0], w["q"].shape[2], 1), dtype=torch.float32, device=DEV)
+    kc0, vc0 = w["k_cache"].clone(), w["v_cache"].clone()
+    ref_out, ref_lse = pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],
+                                         w["block_table"], k=w["k_new"], v=w["v_new"],
+                                         num_splits=7)
+    w["k_cache"].copy_(kc0)
+    w["v_cache"].copy_(vc0)
+    pa.pa_fwd_kvcache_noalloc(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"], out,
+                              block_table=w["block_table"], k=w["k_new"], v=w["v_new"], lse=lse,
+                              num_splits=7)
+    torch.cuda.synchronize()
+    assert float(np.abs(np64(out) - np64(ref_out)).max()) <= OUT_TOL[dt]
+    assert float((lse - ref_lse).abs().max()) <= LSE_TOL
+    strided = torch.empty((w["k_new"].shape[0], w["k_new"].shape[1], w["k_new"].shape[2],
+                           2 * w["k_new"].shape[3]), dtype=w["k_new"].dtype, device=DEV)
+    k_view = strided[..., :w["k_new"].shape[3]]
+    assert not k_view.is_contiguous()
+    with pytest.raises(ValueError):
+        pa.pa_fwd_kvcache_noalloc(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"], out,
+                                  block_table=w["block_table"], k=k_view, v=w["v_new"], lse=lse)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib = pa.load_library()
     # 256 sequences x 64 q heads at D 128 with 128 forced splits need about
     # 1 GB of split scratch, far beyond the fixed array: rejected with a clear
-    # error before any work is queued.
+    # error before any work is queued.  Every pointer is NULL, so that even if
+    # the size check came later the call would stop at argument validation.
     need = lib.pa_fwd_kvcache_workspace_size(256, 1, 64, 8, 128, 131072, 128)
     assert need > pa.PA_NOALLOC_SCRATCH_BYTES
-    t4 = pa.pa_tensor4(4096, 1 << 20, 1024, 128)
-    rc = lib.pa_fwd_kvcache_noalloc(4096, 64 * 128, 64 * 128, 128, t4, t4, None, None, 0, 4096,
-                                    4096, 8192, 8192, 16, 256, 1, 64, 8, 128, 1 << 16, 131072,
-                                    1.0 / math.sqrt(128), 0, 128, 4096, None, None, pa.PA_F16,
+    t4 = pa.pa_tensor4(None, 1 << 20, 1024, 128)
+    rc = lib.pa_fwd_kvcache_noalloc(None, 64 * 128, 64 * 128, 128, t4, t4, None, None, 0, None,
+                                    None, 8192, 8192, 16, 256, 1, 64, 8, 128, 1 << 16, 131072,
+                                    1.0 / math.sqrt(128), 0, 128, None, None, None, pa.PA_F16,
                                     None)
     assert rc == pa.PA_ERR_WORKSPACE
     assert "scratch" in lib.pa_last_error_string().decode()
