@@ -216,13 +216,15 @@ def test_full_size_decode_sweep_point_sampled():
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("hq,hkv,lq,splits", [(32, 8, 1, 0), (64, 8, 1, 0), (16, 4, 2, 3),
-                                              (12, 4, 1, 5), (8, 1, 1, 0), (6, 2, 2, 0)])
+                                              (12, 4, 1, 5), (8, 1, 1, 0), (6, 2, 2, 0),
+                                              (32, 8, 6, 0), (16, 2, 4, 3), (12, 4, 7, 0)])
 def test_gqa_rows_share_each_key(dtype, d, hq, hkv, lq, splits):
-    """3-8 query rows per kv head (GQA decode, short multi-query decode with a
-    causal in-call append): the CUDA-core decode layout that reduce-scatters
-    the rows' dot products, including padded row counts (3 and 6 of 4 and 8),
-    ragged lengths whose last page is partial, and forced split counts."""
-    lens = [1000, 37, 700, 16, 2, 513]
+    """3-32 query rows per kv head (GQA decode, multi-query decode with a
+    causal in-call append): up to 16 rows the decode kernel's warp-level
+    tensor-core consumer (8 rows per MMA tile; padded row counts 3 and 6),
+    past 16 the tcgen05 engine's packed items (21, 24 and 32 rows); ragged
+    lengths whose last page is partial, and forced split counts."""
+    lens = [1000, 37, 700, 16, 8, 513]
     w = wl.paged_decode(len(lens), 0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, lens=lens,
                         lnew=lq, seed=31 + hq + lq + d, device=DEV, dtype=dtype)
     w["causal"] = lq > 1
