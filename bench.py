@@ -111,7 +111,7 @@ def time_calls(fn, steps, warmup, stream, graph=True, flush=False):
     `flush`, every call is preceded by an L2 flush (L2Flush) outside its own
     event pair: for workloads whose inputs would otherwise stay in L2 between
     calls; the call's launches are queued behind the flush, so no host gap
-    shows up inside the pair."""
+    shows up inside the pair, and the figure is the mean over the pairs."""
     import torch
 
     for _ in range(warmup):
@@ -129,6 +129,10 @@ def time_calls(fn, steps, warmup, stream, graph=True, flush=False):
             fn()
             b.record(stream)
         torch.cuda.synchronize()
+        # the mean, not the median: event timestamps on this part step in
+        # 4.096 us, so a single call's time is a multiple of that and the
+        # median of such samples snaps to one of the multiples; calls that
+        # start at random phases against the step average to the true time
         return sum(a.elapsed_time(b) for a, b in pairs) / steps * 1e3
     if graph:
         g = torch.cuda.CUDAGraph()
@@ -180,6 +184,7 @@ def sweep_point(dev, ctx, B, peak):
     if by < 4 * 129e6:
         l2flush = L2Flush(dev)
         ts = []
+        steps = max(steps, 60)  # enough calls to average out the timestamp step
         for i in range(steps + 3):
             l2flush()
             e0 = torch.cuda.Event(enable_timing=True)
@@ -190,7 +195,7 @@ def sweep_point(dev, ctx, B, peak):
             e1.synchronize()
             if i >= 3:
                 ts.append(e0.elapsed_time(e1) * 1e3)
-        us = statistics.median(ts)
+        us = sum(ts) / len(ts)  # mean: see time_calls on the 4.096 us timestamp step
         mode = "cold (L2 flushed per call)"
         del l2flush
     else:

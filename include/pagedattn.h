@@ -5,8 +5,8 @@
  * What it computes: O = softmax(scale * Q K^T) V per query head, optionally
  * causal (bottom-right aligned: query row i of Lq sees keys t <= i + Lk - Lq),
  * for MHA and GQA (query head h reads kv head h / (Hq/Hkv)).  K and V are read
- * through a per-sequence block table of 16-token pages, with per-sequence
- * lengths taken from device arrays -- the flash_attn_with_kvcache /
+ * through a per-sequence block table of pages of 16 to 256 tokens (or from a
+ * contiguous cache), with per-sequence lengths taken from device arrays -- the flash_attn_with_kvcache /
  * flash_attn_varlen_func interface discussed on
  *   flash-attention #824 "Add support for small page sizes" (reproduction
  *     snippet; page size 16; k=/v= append through block_table),

@@ -71,12 +71,20 @@ int plan_s_max(int B, int Hkv, int max_seqlen_k, int num_splits) {
   return std::max(1, s);
 }
 
-// Would the device split schedule (split-KV schedule in pa_common.cuh) split
-// anything for B sequences of the capacity max_seqlen_k?  The same candidate
-// costs, evaluated on the host for uniform lengths at that bound: when even
-// then one split per sequence wins, the call runs unsplit (no schedule, no
-// combine launch), which is what the device would choose for lengths at the
-// bound and costs at most the split gain of shorter, ragged batches.
+// Host gate of the automatic split: may the device's balanced schedule (equal
+// page shares over all streams, see decode.cu) pay for its partial writes
+// and in-launch merge, for B sequences of the capacity max_seqlen_k?  When it
+// cannot, the call runs one split per stream (no schedule, no partials).
+// Two tests, both on capacities only:
+//   - whole splits per sequence: the cheapest of n in {1..16} splits per
+//     stream, costed as rounds of items over the resident CTAs times (pages
+//     per item + 4); a split plan must beat the unsplit one by 3 % (its
+//     one-unit wins, such as a 32-page capacity cut in four, do not pay);
+//   - balance: streams of at least 128 pages (2048 keys) whose unsplit last
+//     round leaves at least a tenth of the CTA rounds idle, when equal shares
+//     save at least 32 pages per CTA (measured, 32 kv heads: ctx 4096 x B8
+//     and ctx 2048 x B16 save 40 pages and run 3.6 / 4.2 % faster; ctx 2048
+//     x B8 saves 20 and runs 7 % slower, the split's fixed cost).
 bool decode_splits_useful(int B, int Hkv, int max_seqlen_k, int s_max, int target_ctas) {
   if (s_max <= 1 || target_ctas < 1) return false;
   const int P = std::max(1, (max_seqlen_k + kPage - 1) / kPage);
@@ -99,10 +107,14 @@ bool decode_splits_useful(int B, int Hkv, int max_seqlen_k, int s_max, int targe
       best_n = k;
     }
   }
-  // a split plan must beat the unsplit one by at least 3 %: the model's
-  // one-unit wins (a 32-page capacity cut in four) do not pay for the combine
-  // launch (measured: tiny decode 11.0 -> 6.0 us, ctx 512 x B1/B2 -11 / -20 %)
-  return best_n > 1 && best * 100 <= unsplit * 97;
+  // (23 pages: the split's fixed cost, fitted when the merge was a second
+  // launch; measured then: tiny decode 11.0 -> 6.0 us unsplit, ctx 512 x
+  // B1 / B2 -11 / -20 %)
+  if (best_n > 1 && best * 100 <= unsplit * 97) return true;
+  const long long streams = (long long)B * Hkv;
+  const long long rounds = (streams + target_ctas - 1) / target_ctas;
+  const long long share = (streams * P + target_ctas - 1) / target_ctas;
+  return P >= 128 && rounds * target_ctas * 10 >= streams * 11 && rounds * P - share >= 32;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
