@@ -594,11 +594,8 @@ static int fwd_kvcache_impl(const void* q, int64_t q_sb, int64_t q_st, int64_t q
   p.page_shift = shift;
   p.extent = cache_extent;
   p.cache_seqlens = cache_seqlens;
-  p.cu_seqlens_q = nullptr;
-  p.seqlens_k = nullptr;
   p.B = B; p.Lq = Lq; p.Hq = Hq; p.Hkv = Hkv; p.G = G;
   p.max_seqlen_k = max_seqlen_k;
-  p.total_q = 0;
   p.scale_log2 = scale * kLog2e;
   p.causal = causal ? 1 : 0;
   p.s_max = s_max;

@@ -96,30 +96,18 @@ struct DecodeTraits {
 };
 
 struct SeqInfo {
-  int qlen;     // query rows of this sequence
-  int64_t row0;  // global row index of its first query row (NR addressing)
-  int lk;       // keys attended
-  int old;      // keys already in the cache (kvcache); == lk in varlen mode
-  bool active;  // has decode work (varlen: rows * G <= RMAX)
+  int qlen;      // query rows of this sequence (Lq)
+  int64_t row0;  // row index of its first query row in [B * Lq]
+  int lk;        // keys attended
+  int old;       // keys already in the cache
 };
 
-template <int RMAX>
 __device__ __forceinline__ SeqInfo seq_info(const DecodeParams& p, int b, bool report_errors) {
   SeqInfo si;
-  if (p.cu_seqlens_q != nullptr) {
-    const int q0 = __ldg(p.cu_seqlens_q + b), q1 = __ldg(p.cu_seqlens_q + b + 1);
-    si.qlen = q1 - q0;
-    si.row0 = q0;
-    si.lk = __ldg(p.seqlens_k + b);
-    si.old = si.lk;
-    si.active = si.qlen > 0 && si.qlen * p.G <= RMAX;
-  } else {
-    si.qlen = p.Lq;
-    si.row0 = (int64_t)b * p.Lq;
-    si.old = __ldg(p.cache_seqlens + b);
-    si.lk = si.old + p.Lnew;
-    si.active = true;
-  }
+  si.qlen = p.Lq;
+  si.row0 = (int64_t)b * p.Lq;
+  si.old = __ldg(p.cache_seqlens + b);
+  si.lk = si.old + p.Lnew;
   bool bad = si.old < 0 || si.lk < 0 || si.lk > p.max_seqlen_k || si.qlen < 0;
   if (p.block_table != nullptr) {
     bad = bad || (((int64_t)(si.lk + kPage - 1) / kPage + (1 << p.page_shift) - 1) >> p.page_shift) >
@@ -364,10 +352,7 @@ __device__ __forceinline__ void merge_split_row(const DecodeParams& p, int64_t r
   }
   if (p.lse != nullptr && lane == 0) {
     const float lse_v = L > 0.f ? (M + lg2(L)) * kLn2 : neg_inf();
-    if (p.cu_seqlens_q != nullptr)
-      p.lse[(int64_t)h * p.total_q + row] = lse_v;
-    else
-      p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
+    p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
   }
 }
 
@@ -386,7 +371,7 @@ __device__ __forceinline__ void finish_split(const DecodeParams& p, int* sflag, 
   named_barrier(1, nwarps * 32);
   if (*sflag == 0) return;
   __threadfence();  // every split's partial rows are visible past the last arrival
-  const int64_t nrows_all = p.cu_seqlens_q ? (int64_t)p.total_q : (int64_t)p.B * p.Lq;
+  const int64_t nrows_all = (int64_t)p.B * p.Lq;
   for (int r = warp; r < R; r += nwarps) {
     const int qi = r / p.G;
     merge_split_row<D, T>(p, row0 + qi, g * p.G + (r % p.G), qi, b, nb, nrows_all, lane);
@@ -611,7 +596,7 @@ __device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem
         }
     named_barrier(1, Tr::kConsumerWarps * 32);
     const bool to_partial = nb > 1;
-    const int64_t nrows_all = p.cu_seqlens_q ? (int64_t)p.total_q : (int64_t)p.B * p.Lq;
+    const int64_t nrows_all = (int64_t)p.B * p.Lq;
     for (int r = warp; r < R; r += Tr::kConsumerWarps) {
       float M = neg_inf();
 #pragma unroll
@@ -652,12 +637,7 @@ __device__ __forceinline__ void mma_consume(const DecodeParams& p, uint8_t* smem
         } else {
           *reinterpret_cast<uint32_t*>(orow) = E::from_f2(acc[0] * inv, acc[1] * inv);
         }
-        if (p.lse != nullptr && lane == 0) {
-          if (p.cu_seqlens_q != nullptr)
-            p.lse[(int64_t)h * p.total_q + row] = lse_v;
-          else
-            p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
-        }
+        if (p.lse != nullptr && lane == 0) p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
       }
     }
     if (to_partial)
@@ -730,7 +710,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
   //             streams, concatenated sequence by sequence, are cut into equal
   //             contiguous shares of `share` pages, one per CTA; the pieces a
   //             stream is cut into are its splits (consecutive CTAs).
-  const bool direct = p.s_max <= 1 && p.cu_seqlens_q == nullptr;
+  const bool direct = p.s_max <= 1;
   const bool balanced = !direct && p.target_ctas < kForcedSplitTarget && p.s_max >= 2;
   int num_items = 0;   // direct, uniform
   int chunk = 0;       // uniform: pages per split
@@ -741,15 +721,15 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
     num_items = p.B * p.Hkv;
   } else {
     // Lengths of every sequence -> shared memory (item decoding reads them
-    // there; sLk -1: not handled by this kernel), pages -> sPrefix (scratch
-    // until the prefix sum replaces it), and the longest sequence.
+    // there), pages -> sPrefix (scratch until the prefix sum replaces it),
+    // and the longest sequence.
     int* sRed = reinterpret_cast<int*>(sMerge);
     int pmax = 0;
     for (int b = tid; b < p.B; b += Tr::kThreads) {
-      SeqInfo si = seq_info<RMAX>(p, b, true);
-      const int pages = si.active ? (si.lk + kPage - 1) / kPage : -1;
+      const SeqInfo si = seq_info(p, b, true);
+      const int pages = (si.lk + kPage - 1) / kPage;
       sPrefix[b] = pages;
-      sLk[b] = si.active ? si.lk : -1;
+      sLk[b] = si.lk;
       sOld[b] = si.old;
       pmax = max(pmax, pages);
     }
@@ -770,11 +750,10 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
         int v = 0;
         if (b < p.B) {
           const int pages = sPrefix[b];
-          if (balanced) {
-            v = max(pages, 0) * p.Hkv;
-          } else if (pages >= 0) {
+          if (balanced)
+            v = pages * p.Hkv;
+          else
             split_pages_per(sch, pages, chunk, &v);
-          }
         }
         int incl = v;
 #pragma unroll
@@ -804,13 +783,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
       // -inf) are written here, by CTA b mod grid
       for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (sLk[b] != 0) continue;
-        int qlen = p.Lq;
-        int64_t row0 = (int64_t)b * p.Lq;
-        if (p.cu_seqlens_q != nullptr) {
-          row0 = __ldg(p.cu_seqlens_q + b);
-          qlen = __ldg(p.cu_seqlens_q + b + 1) - (int)row0;
-        }
-        const int nrow = qlen * p.Hq;
+        const int64_t row0 = (int64_t)b * p.Lq;
+        const int nrow = p.Lq * p.Hq;
         for (int idx = tid; idx < nrow * (D / 8); idx += Tr::kThreads) {
           const int r = idx / (D / 8), c = idx % (D / 8);
           T* dst = reinterpret_cast<T*>(p.out) + (row0 + r / p.Hq) * p.Hq * D + (r % p.Hq) * D + c * 8;
@@ -819,10 +793,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
         if (p.lse != nullptr) {
           for (int r = tid; r < nrow; r += Tr::kThreads) {
             const int qi = r / p.Hq, h = r % p.Hq;
-            if (p.cu_seqlens_q != nullptr)
-              p.lse[(int64_t)h * p.total_q + row0 + qi] = neg_inf();
-            else
-              p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = neg_inf();
+            p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = neg_inf();
           }
         }
       }
@@ -834,20 +805,13 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
   // sequence from shared memory (validated and reported by the prologue).
   auto seq_of = [&](int b, SeqInfo& si) {
     if (direct) {
-      si = seq_info<RMAX>(p, b, true);
+      si = seq_info(p, b, true);
       return;
     }
-    if (p.cu_seqlens_q != nullptr) {
-      const int q0 = __ldg(p.cu_seqlens_q + b);
-      si.qlen = __ldg(p.cu_seqlens_q + b + 1) - q0;
-      si.row0 = q0;
-    } else {
-      si.qlen = p.Lq;
-      si.row0 = (int64_t)b * p.Lq;
-    }
+    si.qlen = p.Lq;
+    si.row0 = (int64_t)b * p.Lq;
     si.lk = sLk[b];
     si.old = sOld[b];
-    si.active = true;
   };
   // The next work unit of this CTA: sequence b, kv head g, split s of nb,
   // pages [p0, p1).  Returns false when the CTA has none left.
@@ -976,11 +940,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
         if (!rot_q && lane < nq) {
           const int qi = lane / p.G;
           const int h = g * p.G + (lane % p.G);
-          const T* qrow =
-              p.cu_seqlens_q != nullptr
-                  ? reinterpret_cast<const T*>(p.q) + (si.row0 + qi) * p.q_st + (int64_t)h * p.q_sh
-                  : reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb + (int64_t)qi * p.q_st +
-                        (int64_t)h * p.q_sh;
+          const T* qrow = reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb +
+                          (int64_t)qi * p.q_st + (int64_t)h * p.q_sh;
           bulk_load(sQ + (stage * RMAX + lane) * D, qrow, Tr::kQRowBytes, &full[stage]);
         }
         if (lane < Tr::kTensorsPerProducer * kBoxPerT && w < n) {
@@ -1002,11 +963,8 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
               if (e < nq * D) {
                 const int qi = r / p.G;
                 const int h = g * p.G + (r % p.G);
-                const T* qrow = p.cu_seqlens_q != nullptr
-                                    ? reinterpret_cast<const T*>(p.q) + (si.row0 + qi) * p.q_st +
-                                          (int64_t)h * p.q_sh
-                                    : reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb +
-                                          (int64_t)qi * p.q_st + (int64_t)h * p.q_sh;
+                const T* qrow = reinterpret_cast<const T*>(p.q) + (int64_t)b * p.q_sb +
+                                (int64_t)qi * p.q_st + (int64_t)h * p.q_sh;
                 // query row qi is the (Lnew - Lq + qi)-th new token
                 const int pos = si.old + p.Lnew - si.qlen + qi;
                 y[j] = rope_elem<T>(p, qrow, d, pos, rope_pos_ok(p, b, pos, d == 0));
@@ -1266,11 +1224,11 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
             const int h = g * p.G + (r % p.G);
             const int64_t row = si.row0 + qi;  // global row index
             if (to_partial) {
-              float* op = p.o_part + (((int64_t)s * (p.cu_seqlens_q ? p.total_q : (int64_t)p.B * p.Lq) + row) * p.Hq + h) * D;
+              float* op = p.o_part + (((int64_t)s * ((int64_t)p.B * p.Lq) + row) * p.Hq + h) * D;
   #pragma unroll
               for (int e = 0; e < Tr::kPVE; ++e) op[lane * Tr::kPVE + e] = acc[e] * inv;
               if (lane == 0)
-                p.lse_part[((int64_t)s * (p.cu_seqlens_q ? p.total_q : (int64_t)p.B * p.Lq) + row) * p.Hq + h] = lse_v;
+                p.lse_part[((int64_t)s * ((int64_t)p.B * p.Lq) + row) * p.Hq + h] = lse_v;
             } else {
               T* orow = reinterpret_cast<T*>(p.out) + (row * p.Hq + h) * D + lane * Tr::kPVE;
               if constexpr (Tr::kPVE == 4) {
@@ -1281,12 +1239,7 @@ __global__ void __launch_bounds__(DecodeTraits<D, T, RMAX>::kThreads,
               } else {
                 *reinterpret_cast<uint32_t*>(orow) = E::from_f2(acc[0] * inv, acc[1] * inv);
               }
-              if (p.lse != nullptr && lane == 0) {
-                if (p.cu_seqlens_q != nullptr)
-                  p.lse[(int64_t)h * p.total_q + row] = lse_v;
-                else
-                  p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
-              }
+              if (p.lse != nullptr && lane == 0) p.lse[((int64_t)b * p.Hq + h) * p.Lq + qi] = lse_v;
             }
           }
         }
@@ -1312,7 +1265,7 @@ cudaError_t launch_t(const DecodeParams& p, const CUtensorMap& tmk, const CUtens
   }
   int grid = p.grid_ctas;
   long long max_items;
-  if (p.s_max <= 1 && p.cu_seqlens_q == nullptr)
+  if (p.s_max <= 1)
     max_items = (long long)p.B * p.Hkv;
   else
     max_items = (long long)p.B * p.Hkv * (p.s_max < 1 ? 1 : p.s_max);

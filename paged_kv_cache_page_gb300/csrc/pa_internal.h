@@ -14,14 +14,13 @@ constexpr int kPage = 16;  // tokens per page
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Parameters of the split-KV decode path (also the decode part of the unified
-// varlen launch).  Rows of one work item are the Lq_b * G query rows that
-// share one kv head of one sequence.
+// Parameters of the split-KV decode path.  Rows of one work item are the
+// Lq * G query rows that share one kv head of one sequence.
 struct DecodeParams {
   const void* q;
-  int64_t q_sb, q_st, q_sh;  // element strides (varlen: q_sb unused, rows by q_st)
-  void* out;                 // kvcache: [B, Lq, Hq, D]; varlen: [total_q, Hq, D]
-  float* lse;                // kvcache: [B, Hq, Lq]; varlen: [Hq, total_q]; may be null
+  int64_t q_sb, q_st, q_sh;  // element strides of [B, Lq, Hq, D]
+  void* out;                 // [B, Lq, Hq, D]
+  float* lse;                // [B, Hq, Lq]; may be null
   const void* k_new;         // [B, Lnew, Hkv, D] or null
   const void* v_new;
   int Lnew;
@@ -33,16 +32,14 @@ struct DecodeParams {
   int max_pages;
   int page_shift;  // log2(page size / 16): 16-token boxes per table entry = 1 << page_shift
   int64_t extent;  // pages in pool, or tokens per sequence (contiguous)
-  const int32_t* cache_seqlens;  // kvcache mode
-  const int32_t* cu_seqlens_q;   // varlen mode (non-null selects it)
-  const int32_t* seqlens_k;      // varlen mode
-  int B, Lq, Hq, Hkv, G, max_seqlen_k, total_q;
+  const int32_t* cache_seqlens;  // [B] keys already cached
+  int B, Lq, Hq, Hkv, G, max_seqlen_k;
   float scale_log2;  // softmax scale * log2(e)
   int causal;
   int s_max, target_ctas, min_chunk_pages;
   int grid_ctas;     // persistent CTAs launched (resident capacity)
-  float* o_part;     // [s_max, NR, Hq, D] (NR = B*Lq or total_q)
-  float* lse_part;   // [s_max, NR, Hq]
+  float* o_part;     // [s_max, B * Lq, Hq, D]
+  float* lse_part;   // [s_max, B * Lq, Hq]
   // [B, Hkv] arrival words of the in-launch split merge: (launch tag, count)
   unsigned long long* split_ctr;
   int32_t* err;
