@@ -344,27 +344,29 @@ def unified_leg(dev, stream, only, hpeak, tpeak, res):
 
     # unified mixed batch in one launch: prefills of 100/500/1000 query tokens
     # over cached prefixes U[0, 2048] + 64 decodes with contexts U[1024, 4096],
-    # 32 heads x D 128, bf16, causal
-    w = wl.unified_mixed(num_heads=32, head_dim=128, device=dev, seed=1005)
-    out = torch.empty_like(w["q"])
-    ws = torch.empty(max(1, pa.load_library().pa_fwd_varlen_workspace_size(
-        67, w["q"].shape[0], w["max_seqlen_q"], 32, 32, 128, w["max_seqlen_k"])),
-        dtype=torch.uint8, device=dev)
-    fn = lambda: pa.pa_fwd_varlen_unified(w["q"], w["k_cache"], w["v_cache"],  # noqa: E731
-                                          w["cu_seqlens_q"], w["seqlens_k"], w["block_table"],
-                                          w["max_seqlen_q"], w["max_seqlen_k"], out=out,
-                                          workspace=ws, return_lse=False)
-    us = time_calls(fn, 20 if only is None else 3, 5 if only is None else 3, stream)
-    cu = w["cu_seqlens_q"].cpu().tolist()
-    kl = w["seqlens_k"].cpu().tolist()
-    ql = [cu[i + 1] - cu[i] for i in range(len(kl))]
-    by = sum(kl) * 32 * 128 * 2 * 2 + sum(ql) * 32 * 128 * 2 * 2
-    fl = attention_flops(ql, kl, 32, 128, True)
-    res["unified_mixed_32x128"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
-                                   "tflops": round(fl / us / 1e6, 1),
-                                   "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4),
-                                   "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4)}
-    del w, out, ws
+    # bf16, causal; heads x head_dim 32 x 128 (the reported leg), then
+    # 12 x 64 and 64 x 128
+    for heads, hd in ((32, 128), (12, 64), (64, 128)):
+        w = wl.unified_mixed(num_heads=heads, head_dim=hd, device=dev, seed=1005)
+        out = torch.empty_like(w["q"])
+        ws = torch.empty(max(1, pa.load_library().pa_fwd_varlen_workspace_size(
+            67, w["q"].shape[0], w["max_seqlen_q"], heads, heads, hd, w["max_seqlen_k"])),
+            dtype=torch.uint8, device=dev)
+        fn = lambda: pa.pa_fwd_varlen_unified(w["q"], w["k_cache"], w["v_cache"],  # noqa: E731
+                                              w["cu_seqlens_q"], w["seqlens_k"], w["block_table"],
+                                              w["max_seqlen_q"], w["max_seqlen_k"], out=out,
+                                              workspace=ws, return_lse=False)
+        us = time_calls(fn, 20 if only is None else 3, 5 if only is None else 3, stream)
+        cu = w["cu_seqlens_q"].cpu().tolist()
+        kl = w["seqlens_k"].cpu().tolist()
+        ql = [cu[i + 1] - cu[i] for i in range(len(kl))]
+        by = sum(kl) * heads * hd * 2 * 2 + sum(ql) * heads * hd * 2 * 2
+        fl = attention_flops(ql, kl, heads, hd, True)
+        res[f"unified_mixed_{heads}x{hd}"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
+                                              "tflops": round(fl / us / 1e6, 1),
+                                              "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4),
+                                              "frac_tensor_peak": round(fl / us / 1e6 / tpeak, 4)}
+        del w, out, ws
 
 
 def rest_legs(dev, stream, hpeak, res):
