@@ -213,6 +213,20 @@ def test_full_size_decode_sweep_point_sampled():
     assert_close(out, lse, ref_o, ref_l, "f16", rows=rows)
 
 
+@pytest.mark.parametrize("batch,ctx", [(4, 4096), (8, 4096), (16, 2048)])
+def test_graded_sweep_split_points_sampled(batch, ctx):
+    """Graded points of the decode sweep that run the balanced split
+    schedule at their benchmarked size (32/32 heads, D 128, fp16, one
+    appended token, automatic splits): ctx 4096 x B4 by the whole-split cost
+    test, ctx 4096 x B8 and ctx 2048 x B16 by the idle-last-round test of the
+    host gate.  The first and the last two sequences are checked."""
+    w = wl.paged_decode(batch, ctx, lnew=1, seed=1002 + batch, device=DEV)
+    rows = [0, 1, batch - 2, batch - 1]
+    ref_o, ref_l = oracle_kvcache(w, rows=rows)
+    out, lse = run(w)
+    assert_close(out, lse, ref_o, ref_l, "f16", rows=rows)
+
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("hq,hkv,lq,splits", [(32, 8, 1, 0), (64, 8, 1, 0), (16, 4, 2, 3),
