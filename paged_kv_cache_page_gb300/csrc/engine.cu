@@ -55,6 +55,9 @@ template <int NB> __device__ __forceinline__ uint32_t sbuf_par_of(int t) {
   return (uint32_t)((t / NB) & 1);
 }
 constexpr float kRescaleThreshold = 8.0f;
+// Cost of one work item beyond its key tiles, in tiles (epilogue and the next
+// item's set-up: about 5600 SM cycles against about 2800 per tile).
+constexpr int kItemTiles = 2;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
 constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
 constexpr int kWarpTMA = kSoftWarps;        // first TMA producer warp
@@ -342,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- device schedule
   Sched sc;
+  int unit_first = 0, unit_end = 0;  // varlen: this CTA's contiguous run of units
   sc.uniform = p.cu_seqlens_q == nullptr && (p.s_max <= 1 || !(p.Lq > 0 && p.Lq * p.G <= p.pack_rows));
   sc.packed_u = p.cu_seqlens_q == nullptr && p.Lq > 0 && p.Lq * p.G <= p.pack_rows;
   sc.pre0 = pre0;
@@ -371,44 +375,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       sc.chunk = (int)((c + kTilePages - 1) / kTilePages * kTilePages);
     }
     __syncthreads();
+    // cost prefixes over the same unit order, in key tiles (scratch in the
+    // K stages, free before the first tile): varlen batches deal every CTA a
+    // contiguous run of units of equal estimated cost (see wu_first below)
+    int* cp0 = reinterpret_cast<int*>(sK);
+    int* cp1 = cp0 + (kEngineMaxB + 1);
     if (warp == 0) {
-      int carry0 = 0, carry1 = 0;
+      int carry0 = 0, carry1 = 0, ccarry0 = 0, ccarry1 = 0;
       for (int base = 0; base < p.B; base += 32) {
         const int b = base + lane;
-        int c0 = 0, c1 = 0;
+        int c0 = 0, c1 = 0, w0 = 0, w1 = 0;
         if (b < p.B) {
           const SeqI q = seq_of(p, b, false);
           int n = 0;
           if (packed_seq(p, q.qlen)) {
-            packed_split(p, (q.lk + kPage - 1) / kPage, sc.chunk, &n);
+            const int per = packed_split(p, (q.lk + kPage - 1) / kPage, sc.chunk, &n);
             c1 = n * p.Hkv;
+            w1 = c1 * ((per + kTilePages - 1) / kTilePages + kItemTiles);
           } else if (q.qlen > 0) {
-            c0 = ((q.qlen + kBM - 1) / kBM + 1) / 2 * p.Hq;
+            const int qt = (q.qlen + kBM - 1) / kBM;
+            const int pairs = (qt + 1) / 2;
+            c0 = pairs * p.Hq;
+            // key tiles of all query tiles of one head, shared out over its
+            // pairs (the pairing makes them about equal)
+            int tiles = 0;
+            for (int t = 0; t < qt; ++t) {
+              const int qs = t * kBM, nrows = min(kBM, q.qlen - qs);
+              int k1 = q.lk;
+              if (p.causal) k1 = min(q.lk, qs + nrows + q.lk - q.qlen);
+              tiles += (max(0, k1) + kBN - 1) / kBN;
+            }
+            w0 = c0 * ((tiles + pairs - 1) / pairs + 2 * kItemTiles);
           }
           // split count read by the combine step, for EVERY sequence: 0 for
           // sequences written directly (unsplit, query tiles, empty entries)
           if (blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
         }
-        int i0 = c0, i1 = c1;
+        int i0 = c0, i1 = c1, j0 = w0, j1 = w1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y0 = __shfl_up_sync(0xffffffffu, i0, o);
           const int y1 = __shfl_up_sync(0xffffffffu, i1, o);
+          const int z0 = __shfl_up_sync(0xffffffffu, j0, o);
+          const int z1 = __shfl_up_sync(0xffffffffu, j1, o);
           if (lane >= o) {
             i0 += y0;
             i1 += y1;
+            j0 += z0;
+            j1 += z1;
           }
         }
         if (b < p.B) {
           pre0[b] = carry0 + i0 - c0;
           pre1[b] = carry1 + i1 - c1;
+          cp0[b] = ccarry0 + j0 - w0;
+          cp1[b] = ccarry1 + j1 - w1;
         }
         carry0 += __shfl_sync(0xffffffffu, i0, 31);
         carry1 += __shfl_sync(0xffffffffu, i1, 31);
+        ccarry0 += __shfl_sync(0xffffffffu, j0, 31);
+        ccarry1 += __shfl_sync(0xffffffffu, j1, 31);
       }
       if (lane == 0) {
         pre0[p.B] = carry0;
         pre1[p.B] = carry1;
+        cp0[p.B] = ccarry0;
+        cp1[p.B] = ccarry1;
         misc[0] = carry0;
         misc[1] = carry1;
       }
@@ -416,6 +448,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     sc.total0 = misc[0];
     sc.total1 = misc[1];
+    // this CTA's units: those whose cost position (the cost of all units
+    // before them) lies in [cta * share, (cta + 1) * share)
+    const long long wtot = (long long)cp0[p.B] + cp1[p.B];
+    const long long wshare = (wtot + gridDim.x - 1) / gridDim.x;
+    auto unit_at = [&](long long x) -> int {
+      if (x >= wtot) return sc.total0 + sc.total1;
+      const bool k0 = x < cp0[p.B];
+      const int* cp = k0 ? cp0 : cp1;
+      const int* pre = k0 ? pre0 : pre1;
+      const int xi = (int)(k0 ? x : x - cp0[p.B]);
+      const int b = last_le(cp, p.B, xi);
+      const int n = pre[b + 1] - pre[b];
+      const int u = n > 0 ? (cp[b + 1] - cp[b]) / n : 0;
+      const int li = u > 0 ? (xi - cp[b] + u - 1) / u : 0;
+      return (k0 ? 0 : sc.total0) + pre[b] + min(li, n);
+    };
+    unit_first = unit_at((long long)blockIdx.x * wshare);
+    unit_end = unit_at((long long)(blockIdx.x + 1) * wshare);
   }
   // the combine grid that follows may be scheduled now; it waits on the
   // device for this grid's completion before reading any partial
@@ -428,6 +478,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tQ = tO + D;  // Q of the current item, copied from shared memory
   auto tS = [&](int t) { return tbase + (uint32_t)(sbuf(t) * 128); };
   const int total = sc.total0 + sc.total1;
+  // Work-unit halves of this CTA: uniform batches (equal units) deal units
+  // round-robin; varlen batches take the CTA's contiguous run of units of
+  // equal estimated cost, so that sequences of different lengths do not pile
+  // up on some CTAs (measured: average / slowest CTA busy time 0.83 and 0.73
+  // round-robin on the 32 x 128 and 12 x 64 mixed batches).
+  const bool ranged = !sc.uniform;
+  const int wu_first = ranged ? 2 * unit_first : 2 * (int)blockIdx.x;
+  const int wu_end = ranged ? 2 * unit_end : 2 * total;
+  auto wu_next = [&](int wu) {
+    return (ranged || !(wu & 1)) ? wu + 1 : wu + 2 * (int)gridDim.x - 1;
+  };
 
   if (warp >= kWarpTMA && warp < kWarpTMA + kProdWarps) {
     // ======================= TMA producers =======================
@@ -457,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const CUtensorMap* tm_x = is_v ? &tm_v : &tm_k;
     bool failed = false;
     int tctr = 0, a = 0;
-    for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+    for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
@@ -579,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool is_qk = warp == kWarpQK;
     auto kv_par = [](int t) { return (uint32_t)((t / Tr::kStages) & 1); };
     int tctr = 0, a = 0;
-    for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+    for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
@@ -694,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pair_sync = [&]() { named_barrier(1 + quarter, 64); };
     constexpr int kDH = D / 2;  // O columns per half
     int tctr = 0, a = 0;
-    for (int wu = blockIdx.x * 2; wu < total * 2; wu = (wu & 1) ? wu + 2 * (int)gridDim.x - 1 : wu + 1) {
+    for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
       const bool valid = r < it.nrows;
