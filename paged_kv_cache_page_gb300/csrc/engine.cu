@@ -56,8 +56,9 @@ template <int NB> __device__ __forceinline__ uint32_t sbuf_par_of(int t) {
 }
 constexpr float kRescaleThreshold = 8.0f;
 // Cost of one work item beyond its key tiles, in tiles (epilogue and the next
-// item's set-up: about 5600 SM cycles against about 2800 per tile).
-constexpr int kItemTiles = 2;
+// item's set-up: about 5600 SM cycles against about 2800 per tile, plus the Q
+// load; 3 measured best among 1-4 on the mixed batches).
+constexpr int kItemTiles = 3;
 constexpr int kSoftWarps = 8;               // softmax warps (two per TMEM lane quarter)
 constexpr int kProdWarps = 4;               // TMA producer warps (issue throughput is per warp)
 constexpr int kWarpTMA = kSoftWarps;        // first TMA producer warp
@@ -481,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Work-unit halves of this CTA: uniform batches (equal units) deal units
   // round-robin; varlen batches take the CTA's contiguous run of units of
   // equal estimated cost, so that sequences of different lengths do not pile
-  // up on some CTAs (measured: average / slowest CTA busy time 0.83 and 0.73
-  // round-robin on the 32 x 128 and 12 x 64 mixed batches).
+  // up on some CTAs (measured round-robin: average / slowest CTA busy time
+  // 0.83 and 0.73 on the 32 x 128 and 12 x 64 mixed batches).
   const bool ranged = !sc.uniform;
   const int wu_first = ranged ? 2 * unit_first : 2 * (int)blockIdx.x;
   const int wu_end = ranged ? 2 * unit_end : 2 * total;
