@@ -276,6 +276,12 @@ PA_API int pa_fwd_kvcache_noalloc(const void* q, int64_t q_sb, int64_t q_st, int
  *   max_seqlen_q, max_seqlen_k  host-known capacities (grid sizing only).
  *   out [total_q, Hq, D] contiguous; lse fp32 [Hq, total_q] or NULL.
  *   workspace     pa_fwd_varlen_workspace_size(...) bytes.
+ * The tcgen05 engine runs the whole batch in one launch: sequences of up to
+ * 128 query rows per kv head as packed (split-KV) items, longer chunks as
+ * pairs of 128-row query tiles, each CTA taking a contiguous run of work
+ * units of equal estimated cost; when a decode sequence is split, the combine
+ * kernel follows as a programmatic dependent launch.  At most 4096 entries
+ * (B, padding entries included); more return PA_ERR_UNSUPPORTED.
  */
 PA_API int pa_fwd_varlen_unified(const void* q, int64_t q_st, int64_t q_sh, pa_tensor4 k_cache,
                                  pa_tensor4 v_cache, const int32_t* cu_seqlens_q,
