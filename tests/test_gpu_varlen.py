@@ -57,6 +57,21 @@ def test_unified_mixed_batch(heads, d):
     check(w, out, lse, "bf16", seqs=seqs)
 
 
+@pytest.mark.parametrize("prefill_lens,num_decode,heads", [
+    ((), 96, 32),                      # decode entries only
+    ((300, 700, 1200, 64), 0, 16),     # prefill chunks only
+    ((100,), 2, 4),                    # far fewer work units than CTAs
+])
+def test_unified_dealing_extremes(prefill_lens, num_decode, heads):
+    """The engine deals a varlen batch's work units to CTAs in contiguous runs
+    of equal estimated cost: batches of one kind only, and a batch with far
+    fewer units than CTAs (most runs empty), match the oracle."""
+    w = wl.unified_mixed(num_heads=heads, head_dim=128, prefill_lens=prefill_lens,
+                         num_decode=num_decode, device=DEV, seed=1101 + num_decode + heads)
+    out, lse = run(w)
+    check(w, out, lse, "bf16")
+
+
 def test_unified_gqa_and_padding_entries():
     w = wl.unified_mixed(num_heads=16, num_kv_heads=4, head_dim=128, prefill_lens=(7, 40, 300),
                          prefix_hi=700, num_decode=9, ctx_lo=1, ctx_hi=900, pad_to=16,
