@@ -87,3 +87,31 @@ def test_standalone_append_bit_exact(lnew):
     torch.cuda.synchronize()
     assert err[0].item() == 0
     assert np.array_equal(bits(w["k_cache"]), ek) and np.array_equal(bits(w["v_cache"]), ev)
+
+
+@pytest.mark.parametrize("page", [64, 256])
+@pytest.mark.parametrize("d,hq,hkv,lq,dtype", [(64, 32, 4, 1, "f16"), (128, 16, 1, 1, "bf16"),
+                                               (64, 16, 4, 2, "bf16")])
+def test_tensor_core_decode_consumer(page, d, hq, hkv, lq, dtype):
+    """The decode kernel's warp-level tensor-core consumer (8 and 16 query rows
+    per kv head; 64-column 128-byte-swizzled boxes) at pages of 64 and 256
+    tokens: head dims 64 and 128, a causal two-token append, automatic and
+    forced splits."""
+    w = wl.paged_decode(batch=5, ctx=0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                        dtype=dtype, lnew=lq, seed=950 + page + d + hq + lq, device=DEV,
+                        lens=[lq + 1, 300, 1000, 2500, 4100], page_size=page)
+    w["causal"] = lq > 1
+    ref_o, ref_l = oracle_kvcache(w)
+    for splits in (0, 4):
+        out, lse = run_kvcache(w, num_splits=splits)
+        assert_close(out, lse, ref_o, ref_l, dtype)
+
+
+def test_rotary_in_decode_launch_large_pages():
+    """Rotary embedding inside the decode launch (q staged rotated, k rotated
+    where the fused append stores it) with 256-token pages."""
+    from test_gpu_rotary import run_case
+    w = wl.paged_decode(batch=4, ctx=0, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                        dtype="bf16", lnew=2, seed=960, device=DEV, lens=[2, 45, 1500, 3000],
+                        page_size=256)
+    run_case(w, 64, False, causal=True)
