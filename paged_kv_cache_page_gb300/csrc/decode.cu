@@ -273,8 +273,9 @@ __device__ __forceinline__ void patch_new_tokens(const DecodeParams& p, T* kp, T
 // completes a stream also resets its word to (tag, 0): every completed call
 // leaves the words it used at zero arrivals for a replay.  The 48 low bits
 // of %gridid are the tag; 16 bits count up to the split count.  No CTA
-// waits on another: the compare-and-swap loop ends after at most as many
-// rounds as there are splits.
+// waits on another: an arrival's compare-and-swap loop repeats only when
+// another arrival changed the word, so it ends after at most as many rounds
+// as there are splits.
 __device__ __forceinline__ unsigned long long launch_tag() {
   unsigned long long id;
   asm volatile("mov.u64 %0, %%gridid;" : "=l"(id));
@@ -282,29 +283,75 @@ __device__ __forceinline__ unsigned long long launch_tag() {
 }
 
 // One arrival on `word` for this launch; true for the arrival that makes
-// `nb` of them, which leaves the word at (tag, 0).
+// `nb` of them, which leaves the word at (tag, 0).  The common case is one
+// atomic add: a word that already carries this launch's tag counts the
+// arrival.  An add that finds another tag (the first arrival after another
+// launch, or bytes never written) went to a stale value; that arrival then
+// installs (tag, 1) by compare-and-swap, unless another arrival of this
+// launch has installed the tag meanwhile, in which case it adds itself to
+// the installed count.  Every arrival is counted exactly once: by the one
+// successful installation or by an add to a tagged word.
 __device__ __forceinline__ bool arrive_last(unsigned long long* word, unsigned long long tag,
                                             int nb) {
-  unsigned long long cur = atomicAdd(word, 0ull);
-  for (;;) {
-    const unsigned long long cnt = ((cur >> 16) == tag) ? (cur & 0xffffull) : 0ull;
-    const bool last = cnt + 1 >= (unsigned long long)nb;
-    const unsigned long long want = (tag << 16) | (last ? 0ull : cnt + 1);
-    const unsigned long long prev = atomicCAS(word, cur, want);
-    if (prev == cur) return last;
-    cur = prev;
+  const unsigned long long mine = tag << 16;
+  const unsigned long long old = atomicAdd(word, 1ull);
+  unsigned long long cnt;
+  if ((old >> 16) == tag) {
+    cnt = (old & 0xffffull) + 1ull;
+  } else {
+    unsigned long long cur = old + 1ull;
+    for (;;) {
+      const unsigned long long prev = atomicCAS(word, cur, mine | 1ull);
+      if (prev == cur) {
+        cnt = 1ull;
+        break;
+      }
+      if ((prev >> 16) == tag) {
+        cnt = (atomicAdd(word, 1ull) & 0xffffull) + 1ull;
+        break;
+      }
+      cur = prev;
+    }
   }
+  if (cnt < (unsigned long long)nb) return false;
+  atomicExch(word, mine);
+  return true;
 }
 
 // One warp merges the nb split partials of (row, h): O = sum_s w_s O_s / L,
 // w_s = 2^(LSE_s log2 e - M), LSE = (M + log2 L) ln 2.  An empty split
-// (LSE -inf) has weight 0 and its row is not read.
+// (LSE -inf) has weight 0.  The partial rows of the first kPre splits are
+// loaded together with the LSEs (they lie in the workspace for every split
+// index below s_max), so a merge of up to kPre splits waits on one round
+// trip to memory rather than two.
 template <int D, typename T>
-__device__ __forceinline__ void merge_split_row(const DecodeParams& p, int64_t row, int h, int qi,
-                                                int b, int nb, int64_t nrows_all, int lane) {
+__device__ __noinline__ void merge_split_row(const DecodeParams& p, int64_t row, int h, int qi,
+                                             int b, int nb, int64_t nrows_all, int lane) {
   constexpr int kPVE = D / 32;
+  constexpr int kPre = 4;
   const int64_t base = row * p.Hq + h;
   const int64_t sstride = nrows_all * p.Hq;
+  float pre[kPre][kPVE];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    if (j < nb) {
+      const float* op = p.o_part + (j * sstride + base) * D + lane * kPVE;
+      if constexpr (kPVE == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(op));
+        pre[j][0] = x.x;
+        pre[j][1] = x.y;
+        pre[j][2] = x.z;
+        pre[j][3] = x.w;
+      } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(op));
+        pre[j][0] = x.x;
+        pre[j][1] = x.y;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kPVE; ++e) pre[j][e] = 0.f;
+    }
+  }
   float M = neg_inf();
   float my_ls = neg_inf();
   for (int s = lane; s < nb; s += 32) {
@@ -319,7 +366,17 @@ __device__ __forceinline__ void merge_split_row(const DecodeParams& p, int64_t r
   for (int e = 0; e < kPVE; ++e) acc[e] = 0.f;
   float L = 0.f;
   if (M != neg_inf()) {
-    for (int s = 0; s < nb; ++s) {
+#pragma unroll
+    for (int j = 0; j < kPre; ++j) {
+      const float ls = __shfl_sync(0xffffffffu, my_ls, j);
+      if (j < nb && ls != neg_inf()) {
+        const float w = ex2(ls - M);
+        L += w;
+#pragma unroll
+        for (int e = 0; e < kPVE; ++e) acc[e] = fmaf(w, pre[j][e], acc[e]);
+      }
+    }
+    for (int s = kPre; s < nb; ++s) {
       const float ls = s < 32 ? __shfl_sync(0xffffffffu, my_ls, s)
                               : __ldcg(p.lse_part + s * sstride + base) * kLog2e;
       if (ls == neg_inf()) continue;
