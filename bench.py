@@ -295,10 +295,13 @@ def secondary_measurements(dev, only=None):
         gqa_leg(dev, stream, only, hpeak, res)
         if only == "gqa":
             return res
-    unified_leg(dev, stream, only, hpeak, tpeak, res)
-    if only == "unified":
+    if only in (None, "unified"):
+        unified_leg(dev, stream, only, hpeak, tpeak, res)
+        if only == "unified":
+            return res
+    rest_legs(dev, stream, hpeak, res, only)
+    if only == "spec":
         return res
-    rest_legs(dev, stream, hpeak, res)
     res["decode_sweep_graded"] = graded_sweep(dev)
     return res
 
@@ -369,7 +372,7 @@ def unified_leg(dev, stream, only, hpeak, tpeak, res):
         del w, out, ws
 
 
-def rest_legs(dev, stream, hpeak, res):
+def rest_legs(dev, stream, hpeak, res, only=None):
     import torch
 
     import paged_kv_cache_page_gb300 as pa
@@ -383,13 +386,15 @@ def rest_legs(dev, stream, hpeak, res):
     fn = lambda: pa.pa_fwd_kvcache(w["q"], w["k_cache"], w["v_cache"], w["cache_seqlens"],  # noqa: E731
                                    w["block_table"], k=w["k_new"], v=w["v_new"], causal=True,
                                    out=out, return_lse=False)
-    us = time_calls(fn, 50, 5, stream)
+    us = time_calls(fn, 50 if only is None else 3, 5 if only is None else 3, stream)
     by = algorithmic_bytes(64, 4096, 6, 6, 32, 8, 128)
     res["spec_decode_lq6_b64_ctx4096"] = {"us": round(us, 1), "gbs": round(by / us / 1e3, 1),
                                           "frac_hbm_peak": round(by / us / 1e3 / hpeak, 4)}
     del w, out
-    # rotary embedding of the new token (its own kernel ahead of the decode):
-    # the same paged decode step with and without it, B64 x ctx 4096, 32x128, fp16
+    if only == "spec":
+        return
+    # rotary embedding of the new token (inside the decode launch): the same
+    # paged decode step with and without it, B64 x ctx 4096, 32x128, fp16
     w = wl.paged_decode(batch=64, ctx=4096, lnew=1, seed=1011, device=dev)
     out = torch.empty_like(w["q"])
     ang = torch.arange(4096, dtype=torch.float64, device=dev)[:, None] * (
@@ -719,7 +724,7 @@ def main():
                     help="skip the other configurations (prefill, GQA split-KV, tiny decode)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the paged decode sweep (ctx 512..4096 x batch 1..256) instead")
-    ap.add_argument("--only", choices=["prefill", "gqa", "unified", "graded"],
+    ap.add_argument("--only", choices=["prefill", "gqa", "unified", "spec", "graded"],
                     help="time only this secondary leg (for profiling runs)")
     args = ap.parse_args()
     WORKLOAD["batch"], WORKLOAD["ctx"] = args.batch, args.ctx
