@@ -519,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const CUtensorMap* tm_x = is_v ? &tm_v : &tm_k;
     bool failed = false;
     int tctr = 0, a = 0;
+    int issued = 0, q_issued = 0;  // tiles (and items' Q) whose copies were issued
     for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
       const Item it = get_item(p, sc, wu >> 1, wu & 1);
@@ -541,14 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           report(p.err, PA_DEVERR_TIMEOUT, it.b, -1);
           failed = true;
         }
-        mbar_arrive_expect_tx(q_full, Tr::kQBytes);
-        for (int hh = 0; hh < Tr::kHalves; ++hh) {
-          if (it.kind == 0)
-            tma_load_4d(sQ + hh * Tr::kSlab, &tm_q1, q_full, hh * 64, it.head,
-                        it.qcoord + it.qs, it.qb, pol_q);
-          else
-            tma_load_4d(sQ + hh * Tr::kSlab, &tm_q2, q_full, hh * 64, it.head * p.G, it.qcoord,
-                        it.qb, pol_q);
+        if (!failed) {
+          mbar_arrive_expect_tx(q_full, Tr::kQBytes);
+          for (int hh = 0; hh < Tr::kHalves; ++hh) {
+            if (it.kind == 0)
+              tma_load_4d(sQ + hh * Tr::kSlab, &tm_q1, q_full, hh * 64, it.head,
+                          it.qcoord + it.qs, it.qb, pol_q);
+            else
+              tma_load_4d(sQ + hh * Tr::kSlab, &tm_q2, q_full, hh * 64, it.head * p.G,
+                          it.qcoord, it.qb, pol_q);
+          }
+          q_issued = a + 1;
         }
       }
       __syncwarp();
@@ -602,17 +606,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             report(p.err, PA_DEVERR_TIMEOUT, it.b, j);
             failed = true;
           }
-          mbar_arrive_expect_tx(&x_full[s], (uint32_t)(my_count * 2048));
+          if (!failed) mbar_arrive_expect_tx(&x_full[s], (uint32_t)(my_count * 2048));
         }
         __syncwarp();
-        if (issuer)
+        // after a timeout this warp issues no further copy
+        const bool stop = __shfl_sync(0xffffffffu, failed ? 1 : 0, 0) != 0;
+        if (issuer && !stop)
           tma_load_4d(sX + s * Tr::kKVBytes + my_slab * Tr::kSlab + my_page * 2048, tm_x,
                       &x_full[s], my_slab * 64, g, mc2, mc3, pol_kv);
         __syncwarp();
+        if (!stop) issued = Tj + 1;
       }
       tctr += it.ntiles;
       ++a;
     }
+    // Copies in flight must land before the CTA exits, also when a consumer
+    // stopped waiting after a timeout: wait (bounded) for the last stage
+    // loads this warp issued and the last Q.  Each is the latest phase of its
+    // barrier, so the parity test is exact.
+    if (lane == 0) {
+      for (int i = 1; i <= Tr::kStages && i <= issued; ++i) {
+        const int tl = issued - i;
+        mbar_wait(&x_full[tl % Tr::kStages], (uint32_t)((tl / Tr::kStages) & 1));
+      }
+      if (pw == 0 && q_issued >= 1) mbar_wait(q_full, (uint32_t)((q_issued - 1) & 1));
+    }
+    __syncwarp();
   } else if (warp == kWarpMMA || warp == kWarpQK) {
     // ======================= MMA issuers =======================
     // Warp 15 issues every S = Q K^T, warp 14 every O += P V, each from its

@@ -125,3 +125,58 @@ def test_unified_batch_beyond_512_entries():
     seqs = [0, 1, 2] + list(range(3, 123, 7)) + [122]
     check(w, out, lse, "bf16", seqs=seqs)
     assert torch.isfinite(out[:cu[-1]]).all()
+
+
+def permute_sequences(w, order):
+    """The same batch with its sequences in another order (rows of q,
+    cu_seqlens_q, seqlens_k and block-table rows moved together)."""
+    cu = w["cu_seqlens_q"].cpu().tolist()
+    idx = torch.tensor(order, dtype=torch.long, device=w["q"].device)
+    new_cu = [0]
+    for b in order:
+        new_cu.append(new_cu[-1] + cu[b + 1] - cu[b])
+    w2 = dict(w)
+    w2["q"] = torch.cat([w["q"][cu[b]:cu[b + 1]] for b in order])
+    w2["cu_seqlens_q"] = torch.tensor(new_cu, dtype=torch.int32, device=w["q"].device)
+    w2["seqlens_k"] = w["seqlens_k"][idx]
+    w2["block_table"] = w["block_table"][idx]
+    return w2
+
+
+@pytest.mark.parametrize("d,dtype", [(64, "f16"), (128, "bf16"), (128, "f16")])
+def test_unified_core_and_tensor_items_interleaved(d, dtype):
+    """One-row decode entries, multi-row packed entries (chunks of 2-5
+    tokens) and 128-row query tiles, in alternating order: each CTA's
+    contiguous run of units switches item kind many times, with the
+    pipeline state (stage and buffer parities) running on across them; head
+    dim 64 uses the three-stage layout with its own stage-empty barriers."""
+    w = wl.unified_mixed(num_heads=16, head_dim=d, prefill_lens=(300, 2, 3, 5, 2, 4, 170, 3),
+                         prefix_hi=900, num_decode=40, ctx_lo=1, ctx_hi=2500, dtype=dtype,
+                         device=DEV, seed=2024 + d)
+    pre = list(range(8))
+    dec = list(range(8, 48))
+    order = []
+    for i in range(40):
+        order.append(dec[i])
+        if i % 5 == 0 and pre:
+            order.append(pre.pop(0))
+    order += pre
+    w = permute_sequences(w, order)
+    out, lse = run(w)
+    check(w, out, lse, dtype)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_unified_core_items_split(d):
+    """A few long one-row decodes over 4 heads: far fewer (sequence, head)
+    streams than CTAs, so the packed items are split over the keys and their
+    partials (normalised O and LSE) are merged by the combine step."""
+    w = wl.unified_mixed(num_heads=4, head_dim=d, prefill_lens=(3,), prefix_hi=100,
+                         num_decode=5, ctx_lo=2000, ctx_hi=4096, device=DEV, seed=3030 + d)
+    total_q, hq, _ = w["q"].shape
+    B = w["cu_seqlens_q"].numel() - 1
+    nbytes = pa.load_library().pa_fwd_varlen_workspace_size(
+        B, total_q, w["max_seqlen_q"], hq, w["k_cache"].shape[2], d, w["max_seqlen_k"])
+    assert nbytes > 0  # partials exist: the split path runs
+    out, lse = run(w)
+    check(w, out, lse, "bf16")
