@@ -524,6 +524,9 @@ static int fwd_kvcache_impl(const void* q, int64_t q_sb, int64_t q_st, int64_t q
     ep.s_max = s_max;
     ep.target_ctas = num_splits > 0 ? (1 << 30) : 2 * grid;
     ep.min_chunk_pages = num_splits > 0 ? 1 : kMinChunkPages;
+    // automatic splits of packed items: tile-granular shares, split counts per
+    // (sequence, kv head) stream
+    ep.tilebal = (pack && s_max > 1 && num_splits == 0) ? 1 : 0;
     uint8_t* wsb = reinterpret_cast<uint8_t*>(workspace);
     ep.nsplit = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.off_nsplit) : nullptr;
     ep.lse_part = ws.total ? reinterpret_cast<float*>(wsb + ws.off_lse) : nullptr;
@@ -540,8 +543,8 @@ static int fwd_kvcache_impl(const void* q, int64_t q_sb, int64_t q_st, int64_t q
       c.o_part = ep.o_part;
       c.lse_part = ep.lse_part;
       c.nsplit = ep.nsplit;
-      c.ns_stride = 1;
-      c.ns_group = Hq;
+      c.ns_stride = ep.tilebal ? Hkv : 1;  // counts per stream, or per sequence
+      c.ns_group = ep.tilebal ? G : Hq;
       c.S = s_max;
       c.B = B; c.Lq = Lq; c.Hq = Hq;
       c.cu_seqlens_q = nullptr;

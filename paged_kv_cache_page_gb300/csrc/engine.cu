@@ -13,6 +13,11 @@
 //           decode and short chunked prefills.
 // A varlen batch may mix both kinds in one launch: the unified launch of vLLM
 // #6052 "Unify the kernel used in flash attention backend".
+// Dealing: uniform calls without splits round-robin; varlen batches a
+// contiguous run of units of equal estimated cost per CTA; kvcache packed
+// calls with automatic splits (the TB instantiation) an equal share of the
+// concatenated streams' key tiles per CTA, cutting streams at the share
+// boundaries (split counts then kept per stream).
 //
 // CTA = 512 threads (16 warps), one per SM, persistent over items:
 //   warps 0-7  softmax: warps w and w+4 share tile rows 32(w%4).. (their TMEM
@@ -167,10 +172,18 @@ struct Item {
 struct Sched {
   bool uniform;   // kvcache call: every sequence has the same query length
   bool packed_u;  // uniform and packed
+  // tile-granular shares (the engine's TB instantiation, EngineParams::
+  // tilebal): chunk is the share and total1 the positions; CTA c takes
+  // positions [c * share, (c + 1) * share)
   int total0, total1, chunk;
   const int* pre0;
   const int* pre1;
 };
+
+// Key tiles a stream of `lk` keys occupies in the tile-granular position
+// space: its tiles, or one position for a stream without keys (so that
+// exactly one CTA owns it and writes its empty output).
+__device__ __forceinline__ int tb_span(int lk) { return lk > 0 ? (lk + kBN - 1) / kBN : 1; }
 
 __device__ __forceinline__ int last_le(const int* pre, int n, int x) {
   int lo = 0, hi = n;  // last index in [0, n) with pre[idx] <= x
@@ -195,8 +208,45 @@ __device__ __forceinline__ bool empty_half(const Sched& sc, int wu) {
   return (wu & 1) && (sc.uniform ? sc.packed_u : (wu >> 1) >= sc.total0);
 }
 
+template <bool TB>
 __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc, int idx, int u) {
   Item it;
+  if constexpr (TB) {
+    // stream idx = (sequence, kv head); its piece inside this CTA's positions
+    const int b = idx / p.Hkv;
+    it.b = b;
+    it.head = idx - b * p.Hkv;
+    const SeqI q = seq_of(p, b, true);
+    it.qlen = q.qlen;
+    it.lk = q.lk;
+    it.row0 = q.row0;
+    it.qcoord = q.qcoord;
+    it.qb = q.qb;
+    it.qs = 0;
+    const int span = tb_span(q.lk);
+    const int P = sc.pre1[b] + it.head * span;
+    const int share = sc.chunk;
+    const int lo = (int)min((long long)sc.total1, (long long)blockIdx.x * share);
+    const int hi = min(sc.total1, lo + share);
+    const int x0 = max(lo, P), x1 = min(hi, P + span);
+    if (u != 0 || !packed_seq(p, q.qlen) || x0 >= x1) {
+      it.kind = -1;
+      it.nrows = 0;
+      it.k0 = it.k1 = 0;
+      it.split = 0;
+      it.nsplit = 1;
+      it.ntiles = 0;
+      return it;
+    }
+    it.kind = 1;
+    it.nrows = q.qlen * p.G;
+    it.split = x0 / share - P / share;
+    it.nsplit = (P + span - 1) / share - P / share + 1;
+    it.k0 = min((x0 - P) * kBN, q.lk);
+    it.k1 = min((x1 - P) * kBN, q.lk);
+    it.ntiles = it.k1 > it.k0 ? (it.k1 - it.k0 + kBN - 1) / kBN : 0;
+    return it;
+  }
   int b, head, t = 0, s = 0;
   bool packed, null_item = false;
   auto pick_pair = [&](int qt, int pi) {
@@ -281,7 +331,10 @@ __device__ __forceinline__ Item get_item(const EngineParams& p, const Sched& sc,
   return it;
 }
 
-template <int D, typename T>
+// TB: the tile-granular schedule of kvcache packed calls with automatic
+// splits (a separate instantiation, so that the other calls' role loops carry
+// none of its code at the kernel's register cap).
+template <int D, typename T, bool TB>
 __global__ void __launch_bounds__(kThreads, 1)
     engine_kernel(const EngineParams p, const __grid_constant__ CUtensorMap tm_q1,
                   const __grid_constant__ CUtensorMap tm_q2,
@@ -389,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (b < p.B) {
           const SeqI q = seq_of(p, b, false);
           int n = 0;
-          if (packed_seq(p, q.qlen)) {
+          if (TB && packed_seq(p, q.qlen)) {
+            c1 = p.Hkv * tb_span(q.lk);  // key-tile positions of the sequence's streams
+          } else if (packed_seq(p, q.qlen)) {
             const int per = packed_split(p, (q.lk + kPage - 1) / kPage, sc.chunk, &n);
             c1 = n * p.Hkv;
             w1 = c1 * ((per + kTilePages - 1) / kTilePages + kItemTiles);
@@ -410,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // split count read by the combine step, for EVERY sequence: 0 for
           // sequences written directly (unsplit, query tiles, empty entries)
-          if (blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
+          if (!TB && blockIdx.x == 0 && p.nsplit != nullptr) p.nsplit[b] = n > 1 ? n : 0;
         }
         int i0 = c0, i1 = c1, j0 = w0, j1 = w1;
 #pragma unroll
@@ -449,24 +504,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     sc.total0 = misc[0];
     sc.total1 = misc[1];
-    // this CTA's units: those whose cost position (the cost of all units
-    // before them) lies in [cta * share, (cta + 1) * share)
-    const long long wtot = (long long)cp0[p.B] + cp1[p.B];
-    const long long wshare = (wtot + gridDim.x - 1) / gridDim.x;
-    auto unit_at = [&](long long x) -> int {
-      if (x >= wtot) return sc.total0 + sc.total1;
-      const bool k0 = x < cp0[p.B];
-      const int* cp = k0 ? cp0 : cp1;
-      const int* pre = k0 ? pre0 : pre1;
-      const int xi = (int)(k0 ? x : x - cp0[p.B]);
-      const int b = last_le(cp, p.B, xi);
-      const int n = pre[b + 1] - pre[b];
-      const int u = n > 0 ? (cp[b + 1] - cp[b]) / n : 0;
-      const int li = u > 0 ? (xi - cp[b] + u - 1) / u : 0;
-      return (k0 ? 0 : sc.total0) + pre[b] + min(li, n);
-    };
-    unit_first = unit_at((long long)blockIdx.x * wshare);
-    unit_end = unit_at((long long)(blockIdx.x + 1) * wshare);
+    if constexpr (TB) {
+      // Tile-granular shares: the (sequence, kv head) streams' key tiles laid
+      // end to end (pre1: positions before each sequence), every CTA takes
+      // `share` consecutive positions, and a stream cut by a share boundary
+      // runs as split pieces that the combine step merges.  The share is at
+      // least a capacity stream over s_max - 1, so no stream has more than
+      // s_max pieces.
+      const int W = sc.total1;
+      const int tcap = tb_span(p.max_seqlen_k);
+      int share = (W + (int)gridDim.x - 1) / (int)gridDim.x;
+      if (p.s_max > 1) share = max(share, (tcap + p.s_max - 2) / (p.s_max - 1));
+      share = max(share, 1);
+      sc.chunk = share;
+      const int lo = (int)min((long long)W, (long long)blockIdx.x * share);
+      const int hi = min(W, lo + share);
+      auto stream_at = [&](int x) {
+        const int b = last_le(pre1, p.B, x);
+        return b * p.Hkv + (x - pre1[b]) / tb_span(seq_of(p, b, false).lk);
+      };
+      unit_first = lo < hi ? stream_at(lo) : 0;
+      unit_end = lo < hi ? stream_at(hi - 1) + 1 : 0;
+      if (blockIdx.x == 0 && p.nsplit != nullptr) {
+        // pieces per stream, read by the combine step (0: written directly)
+        for (int i = tid; i < p.B * p.Hkv; i += kThreads) {
+          const int b = i / p.Hkv;
+          const SeqI q = seq_of(p, b, false);
+          int n = 0;
+          if (packed_seq(p, q.qlen)) {
+            const int span = tb_span(q.lk);
+            const int P0 = pre1[b] + (i - b * p.Hkv) * span;
+            n = (P0 + span - 1) / share - P0 / share + 1;
+          }
+          p.nsplit[i] = n > 1 ? n : 0;
+        }
+      }
+    } else {
+      // this CTA's units: those whose cost position (the cost of all units
+      // before them) lies in [cta * share, (cta + 1) * share)
+      const long long wtot = (long long)cp0[p.B] + cp1[p.B];
+      const long long wshare = (wtot + gridDim.x - 1) / gridDim.x;
+      auto unit_at = [&](long long x) -> int {
+        if (x >= wtot) return sc.total0 + sc.total1;
+        const bool k0 = x < cp0[p.B];
+        const int* cp = k0 ? cp0 : cp1;
+        const int* pre = k0 ? pre0 : pre1;
+        const int xi = (int)(k0 ? x : x - cp0[p.B]);
+        const int b = last_le(cp, p.B, xi);
+        const int n = pre[b + 1] - pre[b];
+        const int u = n > 0 ? (cp[b + 1] - cp[b]) / n : 0;
+        const int li = u > 0 ? (xi - cp[b] + u - 1) / u : 0;
+        return (k0 ? 0 : sc.total0) + pre[b] + min(li, n);
+      };
+      unit_first = unit_at((long long)blockIdx.x * wshare);
+      unit_end = unit_at((long long)(blockIdx.x + 1) * wshare);
+    }
   }
   // the combine grid that follows may be scheduled now; it waits on the
   // device for this grid's completion before reading any partial
@@ -522,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0, q_issued = 0;  // tiles (and items' Q) whose copies were issued
     for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
-      const Item it = get_item(p, sc, wu >> 1, wu & 1);
+      const Item it = get_item<TB>(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
       const int g = it.kind == 0 ? it.head / p.G : it.head;
       const int pg_begin = it.k0 / kPage;
@@ -662,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tctr = 0, a = 0;
     for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
-      const Item it = get_item(p, sc, wu >> 1, wu & 1);
+      const Item it = get_item<TB>(p, sc, wu >> 1, wu & 1);
       if (it.ntiles == 0) continue;
       if (is_qk) {
         wait(q_full, (uint32_t)(a & 1), 50);
@@ -777,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tctr = 0, a = 0;
     for (int wu = wu_first; wu < wu_end; wu = wu_next(wu)) {
       if (empty_half(sc, wu)) continue;
-      const Item it = get_item(p, sc, wu >> 1, wu & 1);
+      const Item it = get_item<TB>(p, sc, wu >> 1, wu & 1);
       const bool valid = r < it.nrows;
       const bool quarter_live = quarter * 32 < it.nrows;  // any valid row in this quarter
       int qi, h;
@@ -968,19 +1060,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) tc::tmem_dealloc(tbase, Tr::kTmemCols);
 }
 
-template <int D, typename T>
-cudaError_t launch_t(const EngineParams& p, const CUtensorMap& q1, const CUtensorMap& q2,
-                     const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
+template <int D, typename T, bool TB>
+cudaError_t launch_tb(const EngineParams& p, const CUtensorMap& q1, const CUtensorMap& q2,
+                      const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
   using Tr = EngTraits<D>;
   static bool attr = false;
   if (!attr) {
     const cudaError_t e = cudaFuncSetAttribute(
-        engine_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes);
+        engine_kernel<D, T, TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  engine_kernel<D, T><<<grid, kThreads, Tr::kSmemBytes, st>>>(p, q1, q2, tk, tv);
+  engine_kernel<D, T, TB><<<grid, kThreads, Tr::kSmemBytes, st>>>(p, q1, q2, tk, tv);
   return cudaGetLastError();
+}
+
+template <int D, typename T>
+cudaError_t launch_t(const EngineParams& p, const CUtensorMap& q1, const CUtensorMap& q2,
+                     const CUtensorMap& tk, const CUtensorMap& tv, int grid, cudaStream_t st) {
+  return p.tilebal ? launch_tb<D, T, true>(p, q1, q2, tk, tv, grid, st)
+                   : launch_tb<D, T, false>(p, q1, q2, tk, tv, grid, st);
 }
 
 }  // namespace

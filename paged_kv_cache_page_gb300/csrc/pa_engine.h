@@ -30,6 +30,9 @@ struct EngineParams {
   float scale_log2;
   int causal;
   int s_max, target_ctas, min_chunk_pages;  // split plan of packed items
+  int tilebal;       // kvcache packed call with automatic splits: every CTA takes an equal share
+                     // of the concatenated (sequence, kv head) streams' key tiles, cutting
+                     // streams at the share boundaries; split counts are kept per stream
   float* o_part;     // [s_max, rows, Hq, D] normalised split outputs
   float* lse_part;   // [s_max, rows, Hq]
   int32_t* nsplit;   // [B]: splits to combine (0: final output written directly)
