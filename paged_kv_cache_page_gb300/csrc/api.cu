@@ -124,8 +124,9 @@ struct SplitWorkspace {
 };
 
 // Split workspace: a split-bookkeeping region of 8 bytes per (sequence, kv
-// head) -- the decode kernel's arrival words, or the engine's per-sequence
-// split counts (int32) -- then LSE partials [s_max, rows, Hq] and O partials
+// head) -- the decode kernel's arrival words, or the engine's split counts
+// (int32, per sequence, or per (sequence, kv head) stream under tile-granular
+// shares) -- then LSE partials [s_max, rows, Hq] and O partials
 // [s_max, rows, Hq, D] (fp32), each 256-byte aligned.  Nothing in it has to
 // start at any particular value.
 SplitWorkspace split_workspace_layout(int B, int Hkv, long long rows, int Hq, int D, int s_max) {

@@ -201,9 +201,10 @@ __device__ __forceinline__ int last_le(const int* pre, int n, int x) {
 // through L2 together.  Kind-1 units have one item; their second sub-item (and
 // the second of an odd middle pair) is empty (kind -1, no rows, no tiles).
 // Work units are (item index idx, half u) pairs, wu = 2 idx + u, dealt to the
-// CTAs round-robin by idx.  A kind-0 index carries a pair of query tiles
-// (u = 0 and 1); a packed index only u = 0, so its u = 1 half is skipped from
-// the schedule alone, without looking the unit up (every role skips alike).
+// CTAs by idx (the dealing note at the top of this file).  A kind-0 index
+// carries a pair of query tiles (u = 0 and 1); a packed index only u = 0, so
+// its u = 1 half is skipped from the schedule alone, without looking the unit
+// up (every role skips alike).
 __device__ __forceinline__ bool empty_half(const Sched& sc, int wu) {
   return (wu & 1) && (sc.uniform ? sc.packed_u : (wu >> 1) >= sc.total0);
 }

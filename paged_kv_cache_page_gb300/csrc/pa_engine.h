@@ -35,7 +35,8 @@ struct EngineParams {
                      // streams at the share boundaries; split counts are kept per stream
   float* o_part;     // [s_max, rows, Hq, D] normalised split outputs
   float* lse_part;   // [s_max, rows, Hq]
-  int32_t* nsplit;   // [B]: splits to combine (0: final output written directly)
+  int32_t* nsplit;   // [B], or [B, Hkv] under tilebal: splits to combine (0: final output
+                     // written directly)
   int32_t* err;
 };
 
